@@ -1,0 +1,198 @@
+/*
+ * dcp.h - C ABI of the GB300 (sm_103a) decode-context-parallel MLA hot path.
+ *
+ * Decode context parallelism (DCP) splits each request's KV context over D
+ * shards; every shard runs absorbed-MLA decode attention over its own tokens
+ * and returns a partial output plus its log-sum-exp, and an LSE-weighted
+ * combine merges the shards.  On one GPU the D shards are D disjoint token
+ * partitions of one paged latent KV cache resident in HBM.
+ *
+ * Sources (pages on the method):
+ *   [PR50484] "[Kimi-K3] DCP support", vllm-project/vllm pull request 50484:
+ *             Summary (empty-KV-shard masking of the LSE-weighted reduction),
+ *             "CUDA-graph padding follow-up" and the review thread on the
+ *             padding-row mask (rows of seq_len == 0 requests).
+ *   [PRHUB]   prhub.com.cn summary of the same pull request: implementation
+ *             steps 3-4 (interleaved DCP chunking; -inf masking at the source;
+ *             exp2 LSE-weighted merge; zero-weight skip at the consumer;
+ *             16-byte row alignment), key snippet "Decode: latent multi-query
+ *             attention" (forward_mqa returns (latent_out, lse); then
+ *             combine(latent_out, lse, seq_lens, query_start_loc)), risk 2
+ *             (unsupported dtypes are rejected) and risk 4 (timeouts trap in
+ *             the pages' kernel; here they return a status).
+ *   [PR565]   "perf(mla): fuse K3 DCP verification queries",
+ *             local-inference-lab/vllm pull request 565: Summary (the K=3
+ *             verification rows share each KV load) and review follow-up
+ *             (block-table width contract; reject a table narrower than the
+ *             largest local shard).
+ *
+ * Conventions shared by every entry point:
+ *   - All pointers to arrays are DEVICE pointers to caller-owned memory on the
+ *     current CUDA device; the library allocates nothing, keeps no state
+ *     between calls, never synchronises, and enqueues its kernels on
+ *     `stream` (a cudaStream_t; NULL = legacy default stream).  A call
+ *     returns DCP_OK once its kernels are enqueued.
+ *   - Arrays are dense row-major unless a stride argument says otherwise.
+ *     Strides are in ELEMENTS.
+ *   - Host-detectable errors return a status before anything is launched.
+ *     Errors only the device can see (a block id outside the cache, a
+ *     sequence longer than the declared maximum) never trap: the kernel skips
+ *     the offending token and ORs a DCP_DEVERR_* bit into *dev_error when
+ *     dev_error is non-NULL.
+ *   - Latent geometry is fixed: a KV cache row and a query head row are
+ *     DCP_KV_DIM = 576 bf16 values (512 compressed-KV dims followed by 64
+ *     rope dims); values are the first DCP_LATENT_DIM = 512 dims.
+ *   - LSEs are natural logarithms; -inf marks "no tokens".
+ */
+#ifndef DCP_H_
+#define DCP_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define DCP_LATENT_DIM 512
+#define DCP_ROPE_DIM 64
+#define DCP_KV_DIM 576
+#define DCP_MAX_SHARDS 32
+
+/* Device-side error bits ORed into *dev_error. */
+#define DCP_DEVERR_BAD_BLOCK 1    /* a referenced block id is outside [0, num_blocks) */
+#define DCP_DEVERR_SEQ_TOO_LONG 2 /* seq_len > max_seq_len (clamped to max_seq_len) */
+#define DCP_DEVERR_BAD_ROWS 4     /* query_start_loc decreasing, or q_len > max_q_len */
+#define DCP_DEVERR_TIMEOUT 8      /* a bounded on-device wait gave up */
+
+typedef enum {
+  DCP_OK = 0,
+  DCP_ERR_INVALID_ARG = 1,       /* null pointer, negative or inconsistent size */
+  DCP_ERR_UNSUPPORTED_DTYPE = 2, /* output dtype not supported [PRHUB, risk 2] */
+  DCP_ERR_MISALIGNED = 3,        /* pointer or row stride not 16-byte aligned [PRHUB, step 4] */
+  DCP_ERR_TABLE_TOO_NARROW = 4,  /* bt_width < ceil(max_seq_len / block_size) [PR565, review follow-up] */
+  DCP_ERR_WORKSPACE_TOO_SMALL = 5,
+  DCP_ERR_CUDA = 6,              /* a CUDA runtime/driver call failed (launch, attribute query) */
+  DCP_ERR_TIMEOUT = 7            /* reserved for bounded cross-device waits */
+} dcp_status_t;
+
+typedef enum { DCP_DTYPE_BF16 = 0, DCP_DTYPE_F32 = 1 } dcp_dtype_t;
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char* dcp_status_str(dcp_status_t status);
+
+/* Library ABI version (increments when a signature changes). */
+int dcp_version(void);
+
+/*
+ * Token -> shard mapper (host copy of the device code, for tests).
+ * Positions are dealt to the D shards round-robin in runs of `interleave`
+ * tokens (cp_kv_cache_interleave_size): shard(pos) = floor(pos / I) mod D
+ * [PRHUB, implementation step 3].  Returns -1 if D < 1, I < 1 or pos < 0.
+ */
+int32_t dcp_shard_of(int64_t pos, int32_t D, int32_t interleave);
+
+/*
+ * How many of the first L positions shard d owns:
+ *   floor(L / (I D)) * I + clamp(L mod (I D) - d I, 0, I).
+ * Returns -1 on invalid arguments (L < 0, d outside [0, D), D < 1, I < 1).
+ */
+int32_t dcp_local_len(int32_t L, int32_t d, int32_t D, int32_t interleave);
+
+/*
+ * Bytes of device workspace dcp_mla_decode_partial needs for these sizes on
+ * the CURRENT device (the split-KV plan depends on its SM count).  Zero means
+ * `workspace` may be NULL.  Returns (size_t)-1 on invalid arguments.
+ */
+size_t dcp_decode_workspace_size(int32_t B, int32_t T, int32_t H, int32_t D,
+                                 int32_t max_seq_len, int32_t max_q_len);
+
+/*
+ * Absorbed-MLA decode attention split over D context shards.
+ * [PRHUB, snippet "Decode: latent multi-query attention": forward_mqa(q,
+ *  kv_cache, metadata) -> (latent_out, lse) per rank's shard;
+ *  PR50484 Summary and PRHUB step 4: empty shards masked to -inf at source;
+ *  PR565 Summary: verification rows of one request share each KV load.]
+ *
+ * For query row r of request b (rows qsl[b] .. qsl[b+1]-1, q_len = their
+ * count, i = r - qsl[b]) the row's own context length is
+ *   L_r = max(0, seq_lens[b] - (q_len - 1 - i))
+ * (the new tokens are already in the cache).  For each shard d and head h:
+ *   S = { p < L_r : floor(p / interleave) mod D == d }
+ *   s_p = scale * sum_{k<576} q[r,h,k] * kv(p)[k]
+ *   lse_part[d,r,h] = ln sum_{p in S} exp(s_p)
+ *   O_part[d,r,h,v] = sum_{p in S} exp(s_p - lse_part[d,r,h]) * kv(p)[v],  v < 512
+ * where kv(p) is cache row block_table[b, p / block_size] * block_size +
+ * p % block_size.  If S is empty, the row is a padding row (seq_lens[b] == 0)
+ * or r >= qsl[B]: lse_part = -inf and O_part = 0, and no KV is read.
+ *
+ *   q               bf16 [T, H, 576]; row r starts at q + r * q_stride_tok
+ *                   (q_stride_tok >= H * 576, a multiple of 8).
+ *   kv_cache        bf16 [num_blocks, block_size, 576], dense.
+ *   block_table     int32 [B, bt_width], row stride bt_stride (>= bt_width);
+ *                   only columns < ceil(L_r / block_size) are read.
+ *   seq_lens        int32 [B]; 0 marks a CUDA-graph padding request.
+ *   query_start_loc int32 [B + 1], non-decreasing, qsl[0] = 0.
+ *   B, T            requests and query rows (rows past qsl[B] are padding).
+ *   H               heads (1 .. 1024).
+ *   max_seq_len     host-known upper bound of seq_lens (sizes the split plan
+ *                   and the table-width check).
+ *   max_q_len       host-known upper bound of rows per request.
+ *   D, interleave   shard count (1 .. 32) and run length (>= 1).
+ *   scale           softmax scale (1/sqrt(192) for Kimi-K3).
+ *   O_part          fp32 [D, T, H, 512] output.
+ *   lse_part        fp32 [D, T, H] output.
+ *   workspace       device scratch of >= dcp_decode_workspace_size(...) bytes,
+ *                   16-byte aligned; its contents on entry are ignored.
+ *   dev_error       optional int32 device word for DCP_DEVERR_* bits.
+ *   stream          cudaStream_t.
+ *
+ * B == 0 or T == 0 returns DCP_OK without launching anything.
+ */
+dcp_status_t dcp_mla_decode_partial(
+    const void* q, int64_t q_stride_tok,
+    const void* kv_cache, int32_t num_blocks, int32_t block_size,
+    const int32_t* block_table, int32_t bt_width, int64_t bt_stride,
+    const int32_t* seq_lens, const int32_t* query_start_loc,
+    int32_t B, int32_t T, int32_t H, int32_t max_seq_len, int32_t max_q_len,
+    int32_t D, int32_t interleave, float scale,
+    float* O_part, float* lse_part,
+    void* workspace, size_t workspace_bytes,
+    int32_t* dev_error, void* stream);
+
+/*
+ * LSE-weighted combine of D shard partials, with empty-shard and padding-row
+ * masking [north-star formula; PRHUB step 4 "exp2 LSE weighted merge";
+ * PR50484 "CUDA-graph padding follow-up"].
+ *
+ * For each row r and head h: a row whose request has seq_lens == 0 (or that
+ * lies past qsl[B]) is a padding row: out = 0, out_lse = -inf, nothing else
+ * read.  Otherwise E = { d : lse_part[d,r,h] != -inf }; if E is empty the
+ * result is 0 / -inf.  Else, with l_d = lse_part[d,r,h] * log2(e) and
+ * M = max_{d in E} l_d:
+ *   w_d = exp2(l_d - M),  out = sum_E w_d O_part[d,r,h,:] / sum_E w_d,
+ *   out_lse = (M + log2 sum_E w_d) / log2(e).
+ * O_part[d,r,h,:] is not read for d outside E (it may hold stale data/NaN).
+ *
+ *   O_part     fp32 [D, T, H, 512], 16-byte aligned.
+ *   lse_part   fp32 [D, T, H].
+ *   seq_lens, query_start_loc, B, T: as for the decode call.
+ *   H, D       heads (>= 1), shards (1 .. 32).
+ *   out        [T, H, 512] of out_dtype (BF16: round to nearest even; F32),
+ *              16-byte aligned; must not overlap O_part.
+ *   out_lse    fp32 [T, H]; may alias lse_part (the shard-0 slice): every
+ *              LSE of a (row, head) is read before its out_lse is written.
+ *
+ * B == 0 or T == 0 returns DCP_OK without launching anything.
+ */
+dcp_status_t dcp_lse_combine(
+    const float* O_part, const float* lse_part,
+    const int32_t* seq_lens, const int32_t* query_start_loc,
+    int32_t B, int32_t T, int32_t H, int32_t D,
+    void* out, dcp_dtype_t out_dtype, float* out_lse, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DCP_H_ */

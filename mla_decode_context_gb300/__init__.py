@@ -1,0 +1,238 @@
+"""Thin Python binding of libdcp.so (the DCP MLA decode hot path on GB300).
+
+Argument marshalling only: every step of the path runs in the library's CUDA
+kernels.  Functions named like the C entry points take caller-allocated
+torch tensors; ``decode_partial`` and ``lse_combine`` allocate their outputs
+with torch and call the same entry points.  PyTorch provides device memory
+and streams, nothing else.
+
+The library is loaded on first use; if it has not been built the call raises
+(there is no fallback path).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import torch
+
+from .build_lib import LIB as _LIB_PATH
+
+LATENT_DIM = 512
+ROPE_DIM = 64
+KV_DIM = 576
+MAX_SHARDS = 32
+
+DEVERR_BAD_BLOCK = 1
+DEVERR_SEQ_TOO_LONG = 2
+DEVERR_BAD_ROWS = 4
+DEVERR_TIMEOUT = 8
+
+# arithmetic type of the decode contraction (reported by the benchmark)
+COMPUTE_DTYPE = "f32"
+
+DTYPE_BF16 = 0
+DTYPE_F32 = 1
+
+STATUS = {0: "DCP_OK", 1: "DCP_ERR_INVALID_ARG", 2: "DCP_ERR_UNSUPPORTED_DTYPE",
+          3: "DCP_ERR_MISALIGNED", 4: "DCP_ERR_TABLE_TOO_NARROW",
+          5: "DCP_ERR_WORKSPACE_TOO_SMALL", 6: "DCP_ERR_CUDA", 7: "DCP_ERR_TIMEOUT"}
+
+# (name, restype, argtypes) of every symbol include/dcp.h declares
+_P, _I32, _I64, _F, _SZ = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_float, ctypes.c_size_t
+EXPORTS = [
+    ("dcp_status_str", ctypes.c_char_p, [ctypes.c_int]),
+    ("dcp_version", ctypes.c_int, []),
+    ("dcp_shard_of", _I32, [_I64, _I32, _I32]),
+    ("dcp_local_len", _I32, [_I32, _I32, _I32, _I32]),
+    ("dcp_decode_workspace_size", _SZ, [_I32, _I32, _I32, _I32, _I32, _I32]),
+    ("dcp_mla_decode_partial", ctypes.c_int,
+     [_P, _I64, _P, _I32, _I32, _P, _I32, _I64, _P, _P, _I32, _I32, _I32, _I32, _I32, _I32, _I32, _F,
+      _P, _P, _P, _SZ, _P, _P]),
+    ("dcp_lse_combine", ctypes.c_int, [_P, _P, _P, _P, _I32, _I32, _I32, _I32, _P, ctypes.c_int, _P, _P]),
+]
+
+_lib = None
+
+
+class DCPError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        super().__init__("%s returned %s" % (where, STATUS.get(status, status)))
+        self.status = status
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded libdcp.so (raises if it is missing)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(_LIB_PATH):
+            raise RuntimeError("libdcp.so is not built (%s); run __graft_entry__.build()" % _LIB_PATH)
+        l = ctypes.CDLL(_LIB_PATH)
+        for name, res, args in EXPORTS:
+            f = getattr(l, name)
+            f.restype, f.argtypes = res, args
+        _lib = l
+    return _lib
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    if isinstance(stream, torch.cuda.Stream):
+        return ctypes.c_void_p(stream.cuda_stream)
+    return ctypes.c_void_p(int(stream))
+
+
+def _check(st: int, where: str):
+    if st != 0:
+        raise DCPError(st, where)
+
+
+def _need(t: torch.Tensor, name: str, dtype, contiguous=True):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError("%s must be a torch.Tensor" % name)
+    if t.dtype != dtype:
+        raise TypeError("%s must be %s, got %s" % (name, dtype, t.dtype))
+    if not t.is_cuda:
+        raise ValueError("%s must be a CUDA tensor" % name)
+    if contiguous and not t.is_contiguous():
+        raise ValueError("%s must be contiguous" % name)
+
+
+# ----------------------------------------------------------------------------
+# entry points with the C names
+# ----------------------------------------------------------------------------
+def dcp_version() -> int:
+    return lib().dcp_version()
+
+
+def dcp_status_str(status: int) -> str:
+    return lib().dcp_status_str(status).decode()
+
+
+def dcp_shard_of(pos: int, D: int, interleave: int) -> int:
+    return lib().dcp_shard_of(pos, D, interleave)
+
+
+def dcp_local_len(L: int, d: int, D: int, interleave: int) -> int:
+    return lib().dcp_local_len(L, d, D, interleave)
+
+
+def dcp_decode_workspace_size(B: int, T: int, H: int, D: int, max_seq_len: int, max_q_len: int) -> int:
+    n = lib().dcp_decode_workspace_size(B, T, H, D, max_seq_len, max_q_len)
+    if n == ctypes.c_size_t(-1).value:
+        raise DCPError(1, "dcp_decode_workspace_size")
+    return n
+
+
+def dcp_mla_decode_partial(q, kv_cache, block_table, seq_lens, query_start_loc, O_part, lse_part, *,
+                           D: int, interleave: int, scale: float, max_seq_len: int, max_q_len: int,
+                           workspace: Optional[torch.Tensor] = None, dev_error: Optional[torch.Tensor] = None,
+                           stream=None) -> None:
+    """q bf16 [T, H, 576] (rows may be strided), kv_cache bf16 [NB, bs, 576],
+    block_table int32 [B, W] (rows may be strided), seq_lens int32 [B],
+    query_start_loc int32 [B + 1]; writes O_part fp32 [D, T, H, 512] and
+    lse_part fp32 [D, T, H]."""
+    _need(q, "q", torch.bfloat16, contiguous=False)
+    if q.dim() != 3 or q.shape[2] != KV_DIM or q.stride(2) != 1 or q.stride(1) != KV_DIM:
+        raise ValueError("q must be [T, H, 576] with contiguous heads")
+    _need(kv_cache, "kv_cache", torch.bfloat16)
+    if kv_cache.dim() != 3 or kv_cache.shape[2] != KV_DIM:
+        raise ValueError("kv_cache must be [num_blocks, block_size, 576]")
+    _need(block_table, "block_table", torch.int32, contiguous=False)
+    if block_table.dim() != 2 or block_table.stride(1) != 1:
+        raise ValueError("block_table must be [B, W] with unit column stride")
+    _need(seq_lens, "seq_lens", torch.int32)
+    _need(query_start_loc, "query_start_loc", torch.int32)
+    _need(O_part, "O_part", torch.float32)
+    _need(lse_part, "lse_part", torch.float32)
+    T, H = q.shape[0], q.shape[1]
+    B = seq_lens.shape[0]
+    if query_start_loc.shape[0] != B + 1 or block_table.shape[0] != B:
+        raise ValueError("seq_lens, query_start_loc and block_table disagree on B")
+    if tuple(O_part.shape) != (D, T, H, LATENT_DIM) or tuple(lse_part.shape) != (D, T, H):
+        raise ValueError("O_part must be [D, T, H, 512] and lse_part [D, T, H]")
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = lib().dcp_mla_decode_partial(
+        _ptr(q), q.stride(0), _ptr(kv_cache), kv_cache.shape[0], kv_cache.shape[1], _ptr(block_table),
+        block_table.shape[1], block_table.stride(0), _ptr(seq_lens), _ptr(query_start_loc), B, T, H,
+        max_seq_len, max_q_len, D, interleave, scale, _ptr(O_part), _ptr(lse_part), _ptr(workspace),
+        ws_bytes, _ptr(dev_error), _stream(stream))
+    _check(st, "dcp_mla_decode_partial")
+
+
+def dcp_lse_combine(O_part, lse_part, seq_lens, query_start_loc, out, out_lse, *, stream=None) -> None:
+    """O_part fp32 [D, T, H, 512], lse_part fp32 [D, T, H] -> out [T, H, 512]
+    (bf16 or fp32, by out.dtype) and out_lse fp32 [T, H]."""
+    _need(O_part, "O_part", torch.float32)
+    _need(lse_part, "lse_part", torch.float32)
+    _need(seq_lens, "seq_lens", torch.int32)
+    _need(query_start_loc, "query_start_loc", torch.int32)
+    _need(out_lse, "out_lse", torch.float32, contiguous=False)
+    if out.dtype == torch.bfloat16:
+        dt = DTYPE_BF16
+    elif out.dtype == torch.float32:
+        dt = DTYPE_F32
+    else:
+        raise TypeError("out must be bfloat16 or float32")
+    _need(out, "out", out.dtype)
+    D, T, H = lse_part.shape
+    if tuple(out.shape) != (T, H, LATENT_DIM) or tuple(out_lse.shape) != (T, H):
+        raise ValueError("out must be [T, H, 512] and out_lse [T, H]")
+    if not (out_lse.is_contiguous() or out_lse.data_ptr() == lse_part.data_ptr()):
+        raise ValueError("out_lse must be contiguous")
+    B = seq_lens.shape[0]
+    st = lib().dcp_lse_combine(_ptr(O_part), _ptr(lse_part), _ptr(seq_lens), _ptr(query_start_loc), B, T, H,
+                               D, _ptr(out), dt, _ptr(out_lse), _stream(stream))
+    _check(st, "dcp_lse_combine")
+
+
+# ----------------------------------------------------------------------------
+# allocating conveniences
+# ----------------------------------------------------------------------------
+def decode_workspace(B: int, T: int, H: int, D: int, max_seq_len: int, max_q_len: int,
+                     device=None) -> Optional[torch.Tensor]:
+    n = dcp_decode_workspace_size(B, T, H, D, max_seq_len, max_q_len)
+    if n == 0:
+        return None
+    return torch.empty(n, dtype=torch.uint8, device=device or "cuda")
+
+
+def decode_partial(q, kv_cache, block_table, seq_lens, query_start_loc, D: int, interleave: int,
+                   scale: float, max_seq_len: Optional[int] = None, max_q_len: Optional[int] = None,
+                   dev_error: Optional[torch.Tensor] = None, stream=None):
+    """Allocating form: returns (O_part fp32 [D, T, H, 512], lse_part fp32 [D, T, H]).
+
+    ``max_seq_len``/``max_q_len`` default to the bounds implied by the table
+    width and the row count (no device->host copy)."""
+    T, H = q.shape[0], q.shape[1]
+    B = seq_lens.shape[0]
+    if max_seq_len is None:
+        max_seq_len = block_table.shape[1] * kv_cache.shape[1]
+    if max_q_len is None:
+        max_q_len = max(1, T)
+    O = torch.empty((D, T, H, LATENT_DIM), dtype=torch.float32, device=q.device)
+    lse = torch.empty((D, T, H), dtype=torch.float32, device=q.device)
+    ws = decode_workspace(B, T, H, D, max_seq_len, max_q_len, q.device)
+    dcp_mla_decode_partial(q, kv_cache, block_table, seq_lens, query_start_loc, O, lse, D=D,
+                           interleave=interleave, scale=scale, max_seq_len=max_seq_len,
+                           max_q_len=max_q_len, workspace=ws, dev_error=dev_error, stream=stream)
+    return O, lse
+
+
+def lse_combine(O_part, lse_part, seq_lens, query_start_loc, out_dtype=torch.bfloat16, stream=None):
+    """Allocating form: returns (out [T, H, 512] of out_dtype, out_lse fp32 [T, H])."""
+    D, T, H = lse_part.shape
+    out = torch.empty((T, H, LATENT_DIM), dtype=out_dtype, device=O_part.device)
+    out_lse = torch.empty((T, H), dtype=torch.float32, device=O_part.device)
+    dcp_lse_combine(O_part, lse_part, seq_lens, query_start_loc, out, out_lse, stream=stream)
+    return out, out_lse

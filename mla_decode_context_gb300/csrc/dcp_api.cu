@@ -1,0 +1,205 @@
+// C ABI of the DCP MLA hot path: host-side validation, the split-KV plan and
+// kernel launches.  No allocation, no synchronisation, no global state.
+#include "dcp_kernels.h"
+
+#include <cmath>
+#include <cstdint>
+
+using dcp::DecodeArgs;
+using dcp::SplitPlan;
+
+namespace dcp {
+
+namespace {
+constexpr int kTargetCtasPerUnit = 2;  // CTAs the decode spends on one (row, shard, split)
+constexpr int32_t kMinSplitTokens = 256;
+constexpr int32_t kSplitRound = 64;
+constexpr int kMaxSplits = 32;
+
+int current_sm_count() {
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0) {
+    cudaGetLastError();  // clear: no device is not an error for sizing
+    return 152;          // GB300
+  }
+  return sms;
+}
+}  // namespace
+
+// Most splits a (row, shard) pair with up to `lmax` local tokens may use:
+// enough (row, shard, split) units to give every SM work when there are few
+// rows (long-context B=1 decode), never splits shorter than kMinSplitTokens.
+static int64_t split_cap(int32_t T, int32_t D, int64_t lmax, int sm_count) {
+  const int64_t units = static_cast<int64_t>(T) * D * kTargetCtasPerUnit;
+  int64_t want = (sm_count + units - 1) / units;
+  const int64_t cap_len = (lmax + kMinSplitTokens - 1) / kMinSplitTokens;
+  if (want > cap_len) want = cap_len;
+  if (want > kMaxSplits) want = kMaxSplits;
+  return want < 1 ? 1 : want;
+}
+
+// Split-KV plan: pure function of its arguments (and the SM count).
+SplitPlan plan_splits(int32_t T, int32_t D, int32_t I, int32_t max_seq_len, int sm_count) {
+  SplitPlan p{1, kSplitRound};
+  const int32_t lmax = local_len(max_seq_len < 0 ? 0 : max_seq_len, 0, D, I);  // shard 0 is the largest
+  if (lmax <= 0) return p;
+  const int64_t want = split_cap(T, D, lmax, sm_count);
+  int64_t chunk = (lmax + want - 1) / want;
+  chunk = (chunk + kSplitRound - 1) / kSplitRound * kSplitRound;
+  p.chunk = static_cast<int32_t>(chunk);
+  p.splits = static_cast<int32_t>((lmax + chunk - 1) / chunk);  // <= want
+  if (p.splits < 1) p.splits = 1;
+  return p;
+}
+
+size_t split_workspace_bytes(const SplitPlan& p, int32_t T, int32_t H, int32_t D) {
+  if (p.splits <= 1) return 0;
+  const size_t pairs = static_cast<size_t>(p.splits) * D * T * H;
+  size_t bytes = pairs * kLatent * sizeof(float);
+  bytes = (bytes + 255) / 256 * 256;
+  bytes += pairs * sizeof(float);
+  return (bytes + 255) / 256 * 256;
+}
+
+}  // namespace dcp
+
+static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+extern "C" {
+
+const char* dcp_status_str(dcp_status_t s) {
+  switch (s) {
+    case DCP_OK: return "DCP_OK";
+    case DCP_ERR_INVALID_ARG: return "DCP_ERR_INVALID_ARG";
+    case DCP_ERR_UNSUPPORTED_DTYPE: return "DCP_ERR_UNSUPPORTED_DTYPE";
+    case DCP_ERR_MISALIGNED: return "DCP_ERR_MISALIGNED";
+    case DCP_ERR_TABLE_TOO_NARROW: return "DCP_ERR_TABLE_TOO_NARROW";
+    case DCP_ERR_WORKSPACE_TOO_SMALL: return "DCP_ERR_WORKSPACE_TOO_SMALL";
+    case DCP_ERR_CUDA: return "DCP_ERR_CUDA";
+    case DCP_ERR_TIMEOUT: return "DCP_ERR_TIMEOUT";
+  }
+  return "DCP_ERR_UNKNOWN";
+}
+
+int dcp_version(void) { return 1; }
+
+int32_t dcp_shard_of(int64_t pos, int32_t D, int32_t interleave) {
+  if (D < 1 || interleave < 1 || pos < 0) return -1;
+  return dcp::shard_of(pos, D, interleave);
+}
+
+int32_t dcp_local_len(int32_t L, int32_t d, int32_t D, int32_t interleave) {
+  if (L < 0 || D < 1 || interleave < 1 || d < 0 || d >= D) return -1;
+  return dcp::local_len(L, d, D, interleave);
+}
+
+size_t dcp_decode_workspace_size(int32_t B, int32_t T, int32_t H, int32_t D, int32_t max_seq_len,
+                                 int32_t max_q_len) {
+  if (B < 0 || T < 0 || H < 1 || D < 1 || D > DCP_MAX_SHARDS || max_seq_len < 0 || max_q_len < 0)
+    return static_cast<size_t>(-1);
+  if (B == 0 || T == 0) return 0;
+  // Upper bound over every interleave: a shard never owns more than
+  // max_seq_len tokens, and the split count never exceeds split_cap(lmax).
+  const int sms = dcp::current_sm_count();
+  dcp::SplitPlan p{static_cast<int32_t>(dcp::split_cap(T, D, max_seq_len, sms)), 0};
+  return dcp::split_workspace_bytes(p, T, H, D);
+}
+
+dcp_status_t dcp_mla_decode_partial(const void* q, int64_t q_stride_tok, const void* kv_cache,
+                                    int32_t num_blocks, int32_t block_size, const int32_t* block_table,
+                                    int32_t bt_width, int64_t bt_stride, const int32_t* seq_lens,
+                                    const int32_t* query_start_loc, int32_t B, int32_t T, int32_t H,
+                                    int32_t max_seq_len, int32_t max_q_len, int32_t D, int32_t interleave,
+                                    float scale, float* O_part, float* lse_part, void* workspace,
+                                    size_t workspace_bytes, int32_t* dev_error, void* stream) {
+  if (B < 0 || T < 0 || H < 1 || H > 1024 || D < 1 || D > DCP_MAX_SHARDS || interleave < 1 ||
+      max_seq_len < 0 || max_q_len < 1 || !std::isfinite(scale))
+    return DCP_ERR_INVALID_ARG;
+  if (B == 0 || T == 0) return DCP_OK;
+  if (!q || !kv_cache || !block_table || !seq_lens || !query_start_loc || !O_part || !lse_part)
+    return DCP_ERR_INVALID_ARG;
+  if (num_blocks < 1 || block_size < 1 || bt_width < 1 || bt_stride < bt_width ||
+      q_stride_tok < static_cast<int64_t>(H) * DCP_KV_DIM)
+    return DCP_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(kv_cache) || !aligned16(O_part) || (q_stride_tok % 8) != 0)
+    return DCP_ERR_MISALIGNED;
+  if ((static_cast<int64_t>(max_seq_len) + block_size - 1) / block_size > bt_width)
+    return DCP_ERR_TABLE_TOO_NARROW;
+
+  const int sms = dcp::current_sm_count();
+  const dcp::SplitPlan plan = dcp::plan_splits(T, D, interleave, max_seq_len, sms);
+  const size_t need = dcp::split_workspace_bytes(plan, T, H, D);
+  if (need > 0 && (workspace_bytes < need || !workspace)) return DCP_ERR_WORKSPACE_TOO_SMALL;
+  if (need > 0 && !aligned16(workspace)) return DCP_ERR_MISALIGNED;
+
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  DecodeArgs a{};
+  a.q = static_cast<const __nv_bfloat16*>(q);
+  a.q_stride_tok = q_stride_tok;
+  a.kv = static_cast<const __nv_bfloat16*>(kv_cache);
+  a.num_blocks = num_blocks;
+  a.block_size = block_size;
+  a.block_table = block_table;
+  a.bt_width = bt_width;
+  a.bt_stride = bt_stride;
+  a.seq_lens = seq_lens;
+  a.qsl = query_start_loc;
+  a.B = B; a.T = T; a.H = H;
+  a.max_seq_len = max_seq_len; a.max_q_len = max_q_len;
+  a.D = D; a.I = interleave;
+  a.scale = scale;
+  a.plan = plan;
+  a.dev_error = dev_error;
+  float* ws_O = nullptr;
+  float* ws_lse = nullptr;
+  if (plan.splits > 1) {
+    const size_t pairs = static_cast<size_t>(plan.splits) * D * T * H;
+    ws_O = static_cast<float*>(workspace);
+    ws_lse = reinterpret_cast<float*>(static_cast<char*>(workspace) +
+                                      (pairs * DCP_LATENT_DIM * sizeof(float) + 255) / 256 * 256);
+    a.O_dst = ws_O;
+    a.lse_dst = ws_lse;
+  } else {
+    a.O_dst = O_part;
+    a.lse_dst = lse_part;
+  }
+  cudaError_t e = dcp::launch_decode_simt(a, st);
+  if (e != cudaSuccess) return DCP_ERR_CUDA;
+  if (plan.splits > 1) {
+    const int64_t pairs = static_cast<int64_t>(D) * T * H;
+    e = dcp::launch_lse_merge_f32(ws_O, ws_lse, pairs * DCP_LATENT_DIM, pairs, plan.splits, pairs, H,
+                                  nullptr, nullptr, 0, /*row_mask=*/false, O_part, lse_part, st);
+    if (e != cudaSuccess) return DCP_ERR_CUDA;
+  }
+  return DCP_OK;
+}
+
+dcp_status_t dcp_lse_combine(const float* O_part, const float* lse_part, const int32_t* seq_lens,
+                             const int32_t* query_start_loc, int32_t B, int32_t T, int32_t H, int32_t D,
+                             void* out, dcp_dtype_t out_dtype, float* out_lse, void* stream) {
+  if (B < 0 || T < 0 || H < 1 || D < 1 || D > DCP_MAX_SHARDS) return DCP_ERR_INVALID_ARG;
+  if (out_dtype != DCP_DTYPE_BF16 && out_dtype != DCP_DTYPE_F32) return DCP_ERR_UNSUPPORTED_DTYPE;
+  if (B == 0 || T == 0) return DCP_OK;
+  if (!O_part || !lse_part || !seq_lens || !query_start_loc || !out || !out_lse)
+    return DCP_ERR_INVALID_ARG;
+  if (!aligned16(O_part) || !aligned16(out)) return DCP_ERR_MISALIGNED;
+  const int64_t pairs = static_cast<int64_t>(T) * H;
+  // out must not overlap O_part
+  const char* ob = static_cast<const char*>(out);
+  const char* oe = ob + pairs * DCP_LATENT_DIM * (out_dtype == DCP_DTYPE_BF16 ? 2 : 4);
+  const char* pb = reinterpret_cast<const char*>(O_part);
+  const char* pe = pb + static_cast<int64_t>(D) * pairs * DCP_LATENT_DIM * 4;
+  if (ob < pe && pb < oe) return DCP_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e;
+  if (out_dtype == DCP_DTYPE_BF16)
+    e = dcp::launch_lse_merge_bf16(O_part, lse_part, pairs * DCP_LATENT_DIM, pairs, D, pairs, H, seq_lens,
+                                   query_start_loc, B, static_cast<__nv_bfloat16*>(out), out_lse, st);
+  else
+    e = dcp::launch_lse_merge_f32(O_part, lse_part, pairs * DCP_LATENT_DIM, pairs, D, pairs, H, seq_lens,
+                                  query_start_loc, B, true, static_cast<float*>(out), out_lse, st);
+  return e == cudaSuccess ? DCP_OK : DCP_ERR_CUDA;
+}
+
+}  // extern "C"

@@ -1,0 +1,48 @@
+// Internal launch interface between the C ABI (dcp_api.cu) and the kernels.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "dcp_common.cuh"
+
+namespace dcp {
+
+// Everything one decode launch needs (validated by the C ABI).
+struct DecodeArgs {
+  const __nv_bfloat16* q;
+  int64_t q_stride_tok;  // elements between consecutive rows of q
+  const __nv_bfloat16* kv;
+  int32_t num_blocks, block_size;
+  const int32_t* block_table;
+  int32_t bt_width;
+  int64_t bt_stride;
+  const int32_t* seq_lens;
+  const int32_t* qsl;
+  int32_t B, T, H, max_seq_len, max_q_len, D, I;
+  float scale;
+  // Where partials go: O_dst[((s * D + d) * T + r) * H + h][512] with s the
+  // split (s == 0 only when splits == 1, then O_dst = O_part).
+  float* O_dst;
+  float* lse_dst;
+  SplitPlan plan;
+  int32_t* dev_error;
+};
+
+// Generic LSE merge over `nsrc` sources: pair p (flattened) reads
+// lse_src[s * lse_stride + p] and O_src[s * o_stride + p * 512 ...].
+// With row masking, pair p belongs to row p / H and padding rows give 0/-inf.
+cudaError_t launch_lse_merge_bf16(const float* O_src, const float* lse_src, int64_t o_stride,
+                                  int64_t lse_stride, int nsrc, int64_t npairs, int32_t H,
+                                  const int32_t* seq_lens, const int32_t* qsl, int32_t B,
+                                  __nv_bfloat16* out, float* out_lse, cudaStream_t st);
+cudaError_t launch_lse_merge_f32(const float* O_src, const float* lse_src, int64_t o_stride,
+                                 int64_t lse_stride, int nsrc, int64_t npairs, int32_t H,
+                                 const int32_t* seq_lens, const int32_t* qsl, int32_t B,
+                                 bool row_mask, float* out, float* out_lse, cudaStream_t st);
+
+// Reference SIMT decode (fp32 FMA, any geometry).
+cudaError_t launch_decode_simt(const DecodeArgs& a, cudaStream_t st);
+
+}  // namespace dcp

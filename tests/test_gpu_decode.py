@@ -1,0 +1,136 @@
+"""GPU decode (+ combine) parity with the float64 oracle, through the C ABI."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads as wl
+import mla_decode_context_gb300 as dcp
+from tests import gpu_util as G
+
+pytestmark = pytest.mark.gpu
+
+# Sizes the oracle finishes in seconds that still span several tiles, ragged
+# tails, empty shards, padding requests and rows past the last request.
+SMALL = [
+    wl.TINY,
+    wl.DecodeSpec("h128_d8_i1_ragged", seed=31, B=3, seq_lens=(1, 700, 2049), H=128, block_size=64,
+                  D=8, interleave=1),
+    wl.DecodeSpec("h128_d8_i64_blocks", seed=32, B=3, seq_lens=(1500, 333, 64), H=128, block_size=64,
+                  D=8, interleave=64),
+    wl.DecodeSpec("h128_q4_causal_padding", seed=33, B=4, seq_lens=(0, 2, 903, 4), q_len=4, H=128,
+                  block_size=64, D=8, interleave=1, extra_rows=2),
+    wl.DecodeSpec("h128_d1", seed=34, B=2, seq_lens=(300, 17), H=128, block_size=16, D=1, interleave=1),
+    wl.DecodeSpec("h128_d2_i16_bs32", seed=35, B=2, seq_lens=(777, 65), H=128, block_size=32, D=2,
+                  interleave=16),
+    wl.DecodeSpec("h64_d4_i3_unaligned", seed=36, B=2, seq_lens=(250, 40), H=64, block_size=16, D=4,
+                  interleave=3),
+    wl.DecodeSpec("h16_q2_bs16", seed=37, B=3, seq_lens=(5, 1, 60), q_len=2, H=16, block_size=16, D=4,
+                  interleave=1),
+    wl.DecodeSpec("h128_long_split", seed=38, B=1, seq_lens=(9000,), H=128, block_size=64, D=8,
+                  interleave=1),
+]
+
+
+def _full_check(inp, rows=None):
+    t = G.to_device(inp)
+    O, lse, err = G.run_decode(inp, t)
+    assert err == 0
+    out, out_lse = G.run_combine(O, lse, t)
+    O_ref, lse_ref, rows = oracle.decode_partial(inp, rows)
+    O_g = O.cpu().numpy()[:, rows]
+    lse_g = lse.cpu().numpy()[:, rows]
+    G.check_partials(O_g, lse_g, O_ref, lse_ref, inp["name"])
+    _, _, pad = oracle.row_lengths(inp["seq_lens"], inp["query_start_loc"], inp["T"])
+    out_ref, out_lse_ref = oracle.lse_combine(O_ref, lse_ref, pad[rows])
+    G.check_combined(out.float().cpu().numpy()[rows], out_lse.cpu().numpy()[rows], out_ref, out_lse_ref,
+                     pad[rows], inp["name"])
+    return O, lse, out, out_lse
+
+
+@pytest.mark.parametrize("spec", SMALL, ids=lambda s: s.name)
+def test_decode_matches_oracle(spec):
+    _full_check(wl.make_decode_inputs(spec))
+
+
+def test_decode_is_deterministic():
+    inp = wl.make_decode_inputs(SMALL[1])
+    t = G.to_device(inp)
+    a = G.run_decode(inp, t)
+    b = G.run_decode(inp, t)
+    assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
+
+
+def test_strided_rows_match_dense():
+    inp = wl.make_decode_inputs(SMALL[3])
+    t = G.to_device(inp)
+    O, lse, _ = G.run_decode(inp, t)
+    T, H = t["q"].shape[:2]
+    qw = torch.zeros((T, H + 3, 576), dtype=torch.bfloat16, device="cuda")
+    qw[:, :H] = t["q"]
+    tw = torch.full((t["block_table"].shape[0], t["block_table"].shape[1] + 5), -7, dtype=torch.int32,
+                    device="cuda")
+    tw[:, :t["block_table"].shape[1]] = t["block_table"]
+    O2, lse2, _ = G.run_decode(inp, t, q=qw[:, :H], block_table=tw[:, :t["block_table"].shape[1]])
+    assert torch.equal(O, O2) and torch.equal(lse, lse2)
+
+
+def test_empty_batch_is_a_noop():
+    inp = wl.make_decode_inputs(wl.TINY)
+    t = G.to_device(inp)
+    O = torch.full((4, 0, 16, 512), 7.0, device="cuda")
+    lse = torch.full((4, 0, 16), 7.0, device="cuda")
+    dcp.dcp_mla_decode_partial(t["q"][:0], t["kv_cache"], t["block_table"], t["seq_lens"],
+                               t["query_start_loc"], O, lse, D=4, interleave=1, scale=0.1, max_seq_len=37,
+                               max_q_len=1)
+    torch.cuda.synchronize()
+
+
+def test_bad_block_id_is_flagged_not_trapped():
+    spec = wl.DecodeSpec("bad_block", seed=39, B=2, seq_lens=(200, 90), H=16, block_size=16, D=4,
+                         interleave=1)
+    inp = wl.make_decode_inputs(spec)
+    inp["block_table"] = inp["block_table"].copy()
+    inp["block_table"][0, 3] = inp["num_blocks"] + 1000  # referenced column, outside the cache
+    t = G.to_device(inp)
+    O, lse, err = G.run_decode(inp, t)
+    assert err & dcp.DEVERR_BAD_BLOCK
+    assert not torch.isnan(O).any() and not torch.isnan(lse).any()
+    # request 1 is untouched by the bad id
+    O_ref, lse_ref, rows = oracle.decode_partial(inp, [1])
+    G.check_partials(O.cpu().numpy()[:, rows], lse.cpu().numpy()[:, rows], O_ref, lse_ref, "req1")
+
+
+def test_seq_len_above_declared_max_is_flagged():
+    inp = wl.make_decode_inputs(SMALL[7])
+    t = G.to_device(inp)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    dcp.decode_partial(t["q"], t["kv_cache"], t["block_table"], t["seq_lens"], t["query_start_loc"], D=4,
+                       interleave=1, scale=0.1, max_seq_len=50, max_q_len=2, dev_error=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) & dcp.DEVERR_SEQ_TOO_LONG
+
+
+# --- the four decode workloads at full size, sampled rows ------------------
+@pytest.fixture(scope="module")
+def long_inputs():
+    return wl.make_decode_inputs(wl.LONG_120K)
+
+
+def test_long_context_120k(long_inputs):
+    _full_check(long_inputs, rows=[0])
+
+
+def test_batched_b64(tmp_path):
+    inp = wl.make_decode_inputs(wl.BATCHED_B64)
+    seq = inp["seq_lens"]
+    rows = [int(np.argmin(seq)), int(np.argmax(seq)), 5, 40]
+    _full_check(inp, rows=rows)
+
+
+def test_spec_verify_b32():
+    inp = wl.make_decode_inputs(wl.SPEC_VERIFY_B32)
+    seq = inp["seq_lens"]
+    b = int(np.argmax(seq))
+    rows = list(range(4 * b, 4 * b + 4)) + [4 * 7 + 1]
+    _full_check(inp, rows=rows)

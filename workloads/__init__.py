@@ -240,3 +240,18 @@ def make_combine_inputs(D: int, T: int, H: int = COMBINE_H, seed: Optional[int] 
     lse[em] = float("-inf")
     O[:, pm] = float("nan")
     return O, lse, seq_lens, qsl, empty, padding
+
+
+def to_torch(inp: dict, device="cuda") -> dict:
+    """Device copies of a decode workload's arrays (bf16 bits viewed as
+    torch.bfloat16, int32 tables)."""
+    import torch
+
+    def bf16(bits):
+        return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).to(device)
+    return dict(
+        q=bf16(inp["q"]), kv_cache=bf16(inp["kv_cache"]),
+        block_table=torch.from_numpy(inp["block_table"]).to(device),
+        seq_lens=torch.from_numpy(inp["seq_lens"]).to(device),
+        query_start_loc=torch.from_numpy(inp["query_start_loc"]).to(device),
+    )
