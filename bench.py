@@ -301,7 +301,7 @@ def run_gb300(args, spec):
             "metric": METRIC, "value": ws * tokens / (step_ms * 1e-3), "unit": UNIT, "n_gpus": ws,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_ms,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": dcp.COMPUTE_DTYPE, "data": "synthetic",
+            "dtype": dcp.compute_dtype(), "data": "synthetic",
             "config": {"workload": spec.name, "B": B, "seq_len": int(inp["max_seq_len"]), "H": H, "D": D,
                        "interleave": I, "block_size": inp["block_size"], "q_len": mql,
                        "parallelism": "replicas" if ws > 1 else "single",

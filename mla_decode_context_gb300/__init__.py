@@ -29,8 +29,11 @@ DEVERR_SEQ_TOO_LONG = 2
 DEVERR_BAD_ROWS = 4
 DEVERR_TIMEOUT = 8
 
-# arithmetic type of the decode contraction (reported by the benchmark)
-COMPUTE_DTYPE = "f32"
+def compute_dtype() -> str:
+    """Arithmetic type of the decode contraction: bf16 tensor-core MMAs with
+    fp32 accumulation, or fp32 FMA when the CUDA-core kernel is forced
+    (DCP_FORCE_SIMT=1) or the layout has no tensor-core tiling."""
+    return "f32" if os.environ.get("DCP_FORCE_SIMT", "") == "1" else "bf16"
 
 DTYPE_BF16 = 0
 DTYPE_F32 = 1

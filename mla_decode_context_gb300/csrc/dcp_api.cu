@@ -4,6 +4,7 @@
 
 #include <cmath>
 #include <cstdint>
+#include <cstdlib>
 
 using dcp::DecodeArgs;
 using dcp::SplitPlan;
@@ -164,7 +165,10 @@ dcp_status_t dcp_mla_decode_partial(const void* q, int64_t q_stride_tok, const v
     a.O_dst = O_part;
     a.lse_dst = lse_part;
   }
-  cudaError_t e = dcp::launch_decode_simt(a, st);
+  // DCP_FORCE_SIMT=1 selects the CUDA-core reference kernel (A/B checks)
+  const char* force = std::getenv("DCP_FORCE_SIMT");
+  const bool simt = (force && force[0] == '1') || !dcp::decode_tc_supported(a);
+  cudaError_t e = simt ? dcp::launch_decode_simt(a, st) : dcp::launch_decode_tc(a, st);
   if (e != cudaSuccess) return DCP_ERR_CUDA;
   if (plan.splits > 1) {
     const int64_t pairs = static_cast<int64_t>(D) * T * H;

@@ -45,4 +45,11 @@ cudaError_t launch_lse_merge_f32(const float* O_src, const float* lse_src, int64
 // Reference SIMT decode (fp32 FMA, any geometry).
 cudaError_t launch_decode_simt(const DecodeArgs& a, cudaStream_t st);
 
+// Tensor-core decode (tcgen05/TMEM/TMA, 2-CTA clusters).  Supported when
+// H <= 128 and the shard layout tiles into whole TMA boxes: block_size a
+// multiple of D * interleave (runs inside blocks) or interleave a multiple
+// of block_size (whole blocks per run).
+bool decode_tc_supported(const DecodeArgs& a);
+cudaError_t launch_decode_tc(const DecodeArgs& a, cudaStream_t st);
+
 }  // namespace dcp

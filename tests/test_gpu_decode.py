@@ -48,12 +48,23 @@ def _full_check(inp, rows=None):
     return O, lse, out, out_lse
 
 
+@pytest.fixture(params=["tc", "simt"])
+def kernel(request, monkeypatch):
+    """Default path (tensor cores where the layout allows) and the forced
+    CUDA-core reference kernel."""
+    if request.param == "simt":
+        monkeypatch.setenv("DCP_FORCE_SIMT", "1")
+    else:
+        monkeypatch.delenv("DCP_FORCE_SIMT", raising=False)
+    return request.param
+
+
 @pytest.mark.parametrize("spec", SMALL, ids=lambda s: s.name)
-def test_decode_matches_oracle(spec):
+def test_decode_matches_oracle(spec, kernel):
     _full_check(wl.make_decode_inputs(spec))
 
 
-def test_decode_is_deterministic():
+def test_decode_is_deterministic(kernel):
     inp = wl.make_decode_inputs(SMALL[1])
     t = G.to_device(inp)
     a = G.run_decode(inp, t)
@@ -86,8 +97,8 @@ def test_empty_batch_is_a_noop():
     torch.cuda.synchronize()
 
 
-def test_bad_block_id_is_flagged_not_trapped():
-    spec = wl.DecodeSpec("bad_block", seed=39, B=2, seq_lens=(200, 90), H=16, block_size=16, D=4,
+def test_bad_block_id_is_flagged_not_trapped(kernel):
+    spec = wl.DecodeSpec("bad_block", seed=39, B=2, seq_lens=(200, 90), H=128, block_size=16, D=4,
                          interleave=1)
     inp = wl.make_decode_inputs(spec)
     inp["block_table"] = inp["block_table"].copy()
