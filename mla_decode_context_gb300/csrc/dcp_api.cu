@@ -17,7 +17,11 @@ constexpr int32_t kMinSplitTokens = 256;
 constexpr int32_t kSplitRound = 64;
 constexpr int kMaxSplits = 32;
 
+// CTAs one wave of the decode can hold: the tensor-core kernel's resident
+// cluster count x 2 (one CTA per SM), else the SM count, else GB300's 152.
 int current_sm_count() {
+  const int tc = decode_tc_resident_ctas();
+  if (tc > 0) return tc;
   int dev = 0, sms = 0;
   if (cudaGetDevice(&dev) != cudaSuccess ||
       cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0) {
@@ -33,7 +37,7 @@ int current_sm_count() {
 // rows (long-context B=1 decode), never splits shorter than kMinSplitTokens.
 static int64_t split_cap(int32_t T, int32_t D, int64_t lmax, int sm_count) {
   const int64_t units = static_cast<int64_t>(T) * D * kTargetCtasPerUnit;
-  int64_t want = (sm_count + units - 1) / units;
+  int64_t want = sm_count / units;  // whole waves only
   const int64_t cap_len = (lmax + kMinSplitTokens - 1) / kMinSplitTokens;
   if (want > cap_len) want = cap_len;
   if (want > kMaxSplits) want = kMaxSplits;

@@ -50,6 +50,9 @@ cudaError_t launch_decode_simt(const DecodeArgs& a, cudaStream_t st);
 // multiple of D * interleave (runs inside blocks) or interleave a multiple
 // of block_size (whole blocks per run).
 bool decode_tc_supported(const DecodeArgs& a);
+// CTAs of the tensor-core decode resident at once on the current device
+// (0 if unknown); the split plan sizes one wave from it.
+int decode_tc_resident_ctas();
 cudaError_t launch_decode_tc(const DecodeArgs& a, cudaStream_t st);
 
 }  // namespace dcp

@@ -63,11 +63,32 @@ __device__ __forceinline__ void mbar_arrive_remote(uint32_t peer_addr) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(peer_addr) : "memory");
 }
 
+// Relaxed remote arrive: signals without ordering this thread's earlier
+// memory writes (for "slot consumed" signals whose reads have already
+// produced their values).
+__device__ __forceinline__ void mbar_arrive_remote_relaxed(uint32_t peer_addr) {
+  asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(peer_addr) : "memory");
+}
+
 __device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
       "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Non-blocking probe (test_wait never suspends): for event loops that poll
+// several barriers.
+__device__ __forceinline__ bool mbar_peek(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(ok)
       : "r"(smem_u32(bar)), "r"(parity)
@@ -152,6 +173,26 @@ __device__ __forceinline__ void bulk_copy_to_peer(uint32_t dst_peer, const void*
           dst_peer),
       "r"(smem_u32(src)), "r"(bytes), "r"(bar_peer)
       : "memory");
+}
+
+// 16-byte store into the peer CTA's shared memory (`dst_peer` from
+// map_peer) that completes 16 tx bytes on the peer's mbarrier `bar_peer`.
+__device__ __forceinline__ void st_async_peer(uint32_t dst_peer, float4 v, uint32_t bar_peer) {
+  asm volatile(
+      "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(dst_peer),
+      "r"(__float_as_uint(v.x)), "r"(__float_as_uint(v.y)), "r"(__float_as_uint(v.z)), "r"(__float_as_uint(v.w)),
+      "r"(bar_peer)
+      : "memory");
+}
+
+// 16-byte global -> shared copy through L2 (LSU path, bypasses L1).
+__device__ __forceinline__ void cp_async16(uint32_t dst_smem, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst_smem), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
 // ---------------------------------------------------------------------------
@@ -240,6 +281,17 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
       "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]),
       "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
       : "memory");
+}
+
+// ---------------------------------------------------------------------------
+// math
+// ---------------------------------------------------------------------------
+// 2^x with the hardware approximation (PTX ex2.approx.ftz.f32: relative
+// error about 2^-22, subnormal results flushed to zero; ex2(-inf) = +0).
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
 }
 
 // ---------------------------------------------------------------------------
