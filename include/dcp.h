@@ -191,6 +191,34 @@ dcp_status_t dcp_lse_combine(
     int32_t B, int32_t T, int32_t H, int32_t D,
     void* out, dcp_dtype_t out_dtype, float* out_lse, void* stream);
 
+/*
+ * dcp_mla_decode_partial without a workspace argument, for callers that
+ * cannot allocate device memory (their memory is owned and fully reserved by
+ * a host framework, or they are plugins handed only their inputs and
+ * outputs).  The pages have no counterpart: it is a packaging of the same
+ * decode.
+ *
+ * Same arguments, results and errors as dcp_mla_decode_partial, except that
+ * the split-KV scratch comes from a 24 MiB array inside the library (held on
+ * every device that loads it, until the process exits).  A call whose split
+ * plan needs more than 24 MiB (dcp_decode_workspace_size) returns
+ * DCP_ERR_WORKSPACE_TOO_SMALL without launching; H <= 128 always fits on a
+ * GB300.  The first call on a device looks up the array's device address, so
+ * make it before capturing a stream on that device.  All calls share the
+ * array and it keeps the last call's contents (nothing in it needs to start
+ * at zero); calls whose kernels overlap on the GPU race on it, so order them
+ * on one stream or with events.  Allocates nothing.
+ */
+dcp_status_t dcp_mla_decode_partial_noalloc(
+    const void* q, int64_t q_stride_tok,
+    const void* kv_cache, int32_t num_blocks, int32_t block_size,
+    const int32_t* block_table, int32_t bt_width, int64_t bt_stride,
+    const int32_t* seq_lens, const int32_t* query_start_loc,
+    int32_t B, int32_t T, int32_t H, int32_t max_seq_len, int32_t max_q_len,
+    int32_t D, int32_t interleave, float scale,
+    float* O_part, float* lse_part,
+    int32_t* dev_error, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

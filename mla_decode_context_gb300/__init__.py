@@ -54,6 +54,9 @@ EXPORTS = [
      [_P, _I64, _P, _I32, _I32, _P, _I32, _I64, _P, _P, _I32, _I32, _I32, _I32, _I32, _I32, _I32, _F,
       _P, _P, _P, _SZ, _P, _P]),
     ("dcp_lse_combine", ctypes.c_int, [_P, _P, _P, _P, _I32, _I32, _I32, _I32, _P, ctypes.c_int, _P, _P]),
+    ("dcp_mla_decode_partial_noalloc", ctypes.c_int,
+     [_P, _I64, _P, _I32, _I32, _P, _I32, _I64, _P, _P, _I32, _I32, _I32, _I32, _I32, _I32, _I32, _F,
+      _P, _P, _P, _P]),
 ]
 
 _lib = None
@@ -171,6 +174,37 @@ def dcp_mla_decode_partial(q, kv_cache, block_table, seq_lens, query_start_loc, 
         max_seq_len, max_q_len, D, interleave, scale, _ptr(O_part), _ptr(lse_part), _ptr(workspace),
         ws_bytes, _ptr(dev_error), _stream(stream))
     _check(st, "dcp_mla_decode_partial")
+
+
+def dcp_mla_decode_partial_noalloc(q, kv_cache, block_table, seq_lens, query_start_loc, O_part, lse_part, *,
+                                   D: int, interleave: int, scale: float, max_seq_len: int, max_q_len: int,
+                                   dev_error: Optional[torch.Tensor] = None, stream=None) -> None:
+    """The decode for callers that cannot allocate device memory: same
+    arguments and results as dcp_mla_decode_partial, but the split-KV scratch
+    is a fixed 24 MiB array inside the library (shared by all calls, so calls
+    that overlap on the GPU race; the first call on a device must precede
+    any stream capture on it)."""
+    _need(q, "q", torch.bfloat16, contiguous=False)
+    if q.dim() != 3 or q.shape[2] != KV_DIM or q.stride(2) != 1 or q.stride(1) != KV_DIM:
+        raise ValueError("q must be [T, H, 576] with contiguous heads")
+    _need(kv_cache, "kv_cache", torch.bfloat16)
+    _need(block_table, "block_table", torch.int32, contiguous=False)
+    if block_table.dim() != 2 or block_table.stride(1) != 1:
+        raise ValueError("block_table must be [B, W] with unit column stride")
+    _need(seq_lens, "seq_lens", torch.int32)
+    _need(query_start_loc, "query_start_loc", torch.int32)
+    _need(O_part, "O_part", torch.float32)
+    _need(lse_part, "lse_part", torch.float32)
+    T, H = q.shape[0], q.shape[1]
+    B = seq_lens.shape[0]
+    if tuple(O_part.shape) != (D, T, H, LATENT_DIM) or tuple(lse_part.shape) != (D, T, H):
+        raise ValueError("O_part must be [D, T, H, 512] and lse_part [D, T, H]")
+    st = lib().dcp_mla_decode_partial_noalloc(
+        _ptr(q), q.stride(0), _ptr(kv_cache), kv_cache.shape[0], kv_cache.shape[1], _ptr(block_table),
+        block_table.shape[1], block_table.stride(0), _ptr(seq_lens), _ptr(query_start_loc), B, T, H,
+        max_seq_len, max_q_len, D, interleave, scale, _ptr(O_part), _ptr(lse_part), _ptr(dev_error),
+        _stream(stream))
+    _check(st, "dcp_mla_decode_partial_noalloc")
 
 
 def dcp_lse_combine(O_part, lse_part, seq_lens, query_start_loc, out, out_lse, *, stream=None) -> None:
