@@ -221,12 +221,21 @@ def run_gb300(args, spec):
     wsz = dcp.dcp_decode_workspace_size(B, T, H, D, msl, mql)
     work = torch.empty(max(wsz, 16), dtype=torch.uint8, device=dev) if wsz else None
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    derr = torch.zeros(1, dtype=torch.int32, device=dev)
     stream = torch.cuda.current_stream(dev)
+
+    def check_device_flags(where):
+        # a kernel that reported a bad input or a timed-out wait did not do
+        # the work being timed: stop instead of printing a number
+        flags = int(derr.item())
+        if flags:
+            raise SystemExit(f"bench: device error flags 0x{flags:x} after {where}")
 
     def decode():
         dcp.dcp_mla_decode_partial(t["q"], t["kv_cache"], t["block_table"], t["seq_lens"],
                                    t["query_start_loc"], O, lse, D=D, interleave=I, scale=inp["scale"],
-                                   max_seq_len=msl, max_q_len=mql, workspace=work, stream=stream)
+                                   max_seq_len=msl, max_q_len=mql, workspace=work, dev_error=derr,
+                                   stream=stream)
 
     def combine():
         dcp.dcp_lse_combine(O, lse, t["seq_lens"], t["query_start_loc"], out, out_lse, stream=stream)
@@ -235,6 +244,7 @@ def run_gb300(args, spec):
         decode()
         combine()
     torch.cuda.synchronize()
+    check_device_flags("warm-up")
     launches_per_step = 2 + (1 if wsz else 0)
 
     # ---- device-timed steps (inputs resident, L2 flushed before each) ----
@@ -288,6 +298,7 @@ def run_gb300(args, spec):
         torch.cuda.synchronize()
         e2e_ms.append(1e3 * (time.perf_counter() - w0))
     e2e_avg = max_over_ranks(sum(e2e_ms) / len(e2e_ms), dev)
+    check_device_flags("the timed steps")
 
     tokens = kv_tokens(inp)
     peak, peak_kind = peaks()

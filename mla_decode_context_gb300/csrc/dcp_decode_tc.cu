@@ -1,44 +1,54 @@
-// Tensor-core split-KV MLA decode for sm_103a (tcgen05 + TMEM + TMA + DSMEM).
+// Tensor-core split-KV MLA decode for sm_103a (tcgen05 + TMEM + DSMEM).
 //
 // One work unit = (query row r, shard d, split s): all H <= 128 heads of the
-// row (the MMA M dimension) against the split's shard tokens.  A unit runs on
-// a cluster of two CTAs that split the 576 latent dims by 64-dim chunks:
-//   CTA 0: chunks 0-3 = dims [0, 256)        (its value dims [0, 256))
-//   CTA 1: chunks 4-8 = dims [256, 576)      (its value dims [256, 512) and
-//                                             the 64 rope dims)
-// so every KV byte is loaded from HBM exactly once, by exactly one CTA, as a
-// single run of consecutive chunks.  Per 32-token tile:
-//   producers (2)  TMA-load the CTA's chunks of the tile's tokens into a
-//                  stage ring (alternate tiles).  A 5-D tensor map whose chunk dimension comes
-//                  after the row dimensions lets one box carry all of the
-//                  CTA's chunks for a group of rows of one block (a box costs
-//                  tens of cycles to issue whatever it carries);
-//   S warps (3)    S(j) = Q_c K_c^T with Q_c (128 rows x 256 or 320 dims,
-//                  bf16) resident in TMEM: 16 or 20 tcgen05.mma (M=128 N=32
-//                  K=16) into S buffer j mod 3, issued by warp 6 + (j mod 3)
-//                  (a tcgen05.mma occupies its issuing thread far longer than
-//                  an N=32 product takes, so issue is spread over warps);
-//   PV warp        O_c += P(j) V_c in tile order (P bf16 in TMEM, V_c = the
-//                  CTA's first four chunks of the same tiles read MN-major,
-//                  N=256 K=16);
-//   softmax warps  thread = head = TMEM lane: ship the fp32 partial S of tile
-//                  j+1 to the peer CTA (a 4 KB DSMEM bulk copy per warp,
-//                  completing on the peer's mbarrier) before working on tile
-//                  j, add the peer's partial of tile j, online softmax in
-//                  base 2 with a lazy rescale (the running max only moves
-//                  when it grows by more than 2^8), P -> TMEM as bf16 while
-//                  the normaliser sums the fp32 weights.
-// Both CTAs hold the same S, so they take the same softmax decisions; each
-// writes its 256 output dims, CTA 0 the LSE.  No tensor-core work is
-// duplicated.  Every wait is bounded (a timeout sets DCP_DEVERR_TIMEOUT and
-// ends the unit).
+// row (the MMA M dimension) against the split's shard tokens, in tiles of 32
+// tokens.  A unit runs on a cluster of two CTAs with different jobs:
+//   score CTA (rank 0)  holds Q (128 x 576 bf16 = 288 TMEM columns), computes
+//                       S(j) = Q K(j)^T as two halves over dims [0, 288) and
+//                       [288, 576) (18 tcgen05.mma each, M=128 N=32 K=16, A
+//                       from TMEM, issued by two warps into two accumulators
+//                       that the softmax adds), runs the online softmax and
+//                       ships P(j) (bf16, 8 KB) plus each head's running max
+//                       to the value CTA;
+//   value CTA (rank 1)  holds O (128 x 512 fp32 = all 512 TMEM columns),
+//                       rescales O when a running max moves, accumulates
+//                       O += P(j) V(j) (4 tcgen05.mma, N=256 K=16, both
+//                       operands in shared memory) and writes O / l.
+// No tensor-core work is duplicated, and the CTAs are coupled one way only
+// (P and the max go from score to value), so neither waits on a round trip to
+// the other inside the tile loop.
+//
+// Each tile is read from HBM once, half by each CTA: the score CTA loads
+// chunks 0-3 and the rope chunk 8 (20 KB), the value CTA chunks 4-7 (16 KB),
+// with 16-byte cp.async, one shard token per row, straight into the
+// 128B-swizzled chunk-major layout the MMAs read.  Each CTA then forwards the
+// part its peer needs with one 16 KB DSMEM bulk copy (score -> value: chunks
+// 0-3; value -> score: chunks 4-7).  This exchange carries raw latents, so
+// it runs as soon as the rows land and sits on no dependency loop.
+// Row-by-row addressing takes any paging geometry (block size, shard count,
+// interleave); rows that must not be read (past the split, bad block ids)
+// are zero-filled.  (TMA boxes were measured to cost a few hundred cycles
+// of issue each, and the shard-strided rows of small interleaves allow only
+// 8-row boxes, which capped the stream well below HBM bandwidth; a single
+// SM's cp.async stream tops out near 16 B/clk, hence the split.)
+//
+// Warp roles (608 threads):
+//   warps 0-3   score: Q load, then softmax (thread = head = TMEM lane)
+//               value: max tracking and O rescale; epilogue columns 0-255
+//   warps 4-9   score: (4-7 also Q load) S issuers: warp 4 + 2i + k issues
+//                      half k of S for tiles j = i mod 3 into S slot i (a
+//                      tcgen05.mma holds its issuing thread far longer than
+//                      an N=32 product takes, so issue is spread over warps)
+//               value: 4-7 epilogue columns 256-511; 8 forwarder; 9 acks
+//   warp 10     both:  TMEM allocation; score: forwarder; value: PV issuer
+//   warps 11-18 both:  producers (cp.async; the score CTA's wait until Q has
+//                      left stages 0-3 for TMEM)
+// Every wait is bounded (a timeout sets DCP_DEVERR_TIMEOUT and ends the unit).
 #include "dcp_kernels.h"
 #include "dcp_sm100.cuh"
 
 #include <cmath>
 #include <cstring>
-
-#include <cuda.h>
 
 namespace dcp {
 namespace {
@@ -46,57 +56,63 @@ namespace {
 using namespace sm100;
 
 constexpr int kTile = 32;                        // tokens per tile (MMA N of S, K of PV)
-constexpr int kStages = 6;                       // KV stage ring
-constexpr int kSBuf = 3;                         // S buffers in TMEM = exchange slots in smem
+constexpr int kStages = 5;                       // stage ring of each CTA
+constexpr int kNch = 9;                          // 64-dim chunks of a latent row
 constexpr int kChunkBytes = kTile * 128;         // 32 rows x 64 bf16, 128B-swizzled
-constexpr int kMaxChunks = 5;                    // chunks one CTA loads (CTA 1)
-constexpr int kStageBytes = kMaxChunks * kChunkBytes;  // 20 KB
-constexpr int kXBytes = 128 * kTile * 4;         // partial S exchange: 128 rows x 32 fp32
-constexpr int kXWarpBytes = kXBytes / 4;         // one softmax warp's 32 rows
-constexpr int kThreads = 320;                    // warps 0-3 softmax, 4 PV, 5 + 9 producers, 6-8 S
+constexpr int kStageBytes = kNch * kChunkBytes;  // 36 KB
+constexpr int kProdWarp0 = 11, kProdWarps = 8;   // producer warps
+constexpr int kProdThreads = 32 * kProdWarps;
+constexpr int kFwdBytes = 4 * kChunkBytes;       // forwarded each way per tile: 4 chunks
+constexpr int kSBuf = 3;                         // S slots (two 32-column halves each) in TMEM
+constexpr int kPSlots = 4;                       // P slots in the value CTA
+constexpr int kPBytes = 128 * kTile * 2;         // P tile: 128 rows x 32 bf16, 64B-swizzled
+constexpr int kPWarpBytes = kPBytes / 4;         // one softmax warp's 32 rows
+constexpr int kPSlotBytes = 9216;                // P tile + running max per head (+ pad)
+constexpr uint32_t kPTx = kPBytes + 128 * 4;     // bytes that fill one P slot
+constexpr int kThreads = 32 * (kProdWarp0 + kProdWarps);
 constexpr float kRescaleLog2 = 8.0f;
 
 // TMEM columns
-constexpr uint32_t kColQ = 0;     // up to 160 columns: Q_c, 2 bf16 per column
-constexpr uint32_t kColS = 160;   // 3 x 32 columns: partial S / P (bf16, first 16)
-constexpr uint32_t kColO = 256;   // 256 columns: O_c
+constexpr uint32_t kColQ = 0;    // score: 288 columns of Q, 2 bf16 per column
+constexpr uint32_t kColS = 288;  // score: 3 slots x 2 halves x 32 columns of S
+constexpr uint32_t kColO = 0;    // value: 512 columns of O
 constexpr uint32_t kTmemCols = 512;
 
 struct __align__(8) Bars {
-  uint64_t kv_full[kStages], kv_empty[kStages];
-  uint64_t s_full[kSBuf], s_free[kSBuf], p_full[kSBuf];
-  uint64_t xfull[kSBuf], xfree[kSBuf];  // 4 arrivals each (one per softmax warp)
-  uint64_t pv_done[2];                  // PV(j) completes phase j / 2 of pv_done[j & 1]
-  uint64_t o_final;                     // last PV complete
-  uint64_t fin[1 + kSBuf];              // each issuing warp's MMAs complete
-  uint32_t mask[kStages];
+  uint64_t kv_loaded[kStages];  // both: this CTA's own rows of tile j landed (every producer thread)
+  uint64_t kv_full[kStages];    // both: own rows (forwarder's arrival) + the peer's 16 KB landed
+  // s_done: score = stage free for own loads (both halves of S(j) + the value
+  //         CTA's ack that chunks 0-3 of tile j landed there); value = the
+  //         score CTA's stage free for the next forward (both halves of S(j))
+  // v_done: value = stage free for own loads (PV(j) + the score CTA's ack
+  //         that chunks 4-7 landed there); score = the value CTA's stage free
+  //         for the next forward (PV(j))
+  uint64_t s_done[kStages], v_done[kStages];
+  uint64_t s_full[kSBuf];     // score: both halves' commits + the slot's mask
+  uint64_t s_free[kSBuf];     // score: the softmax has read the slot (4 warps)
+  uint64_t q_staged;          // score: Q is in shared memory (threads of warps 0-7)
+  uint64_t q_ready;           // score: Q is in TMEM and stages 0-3 are free again (warps 0-7)
+  uint64_t q_gone;            // value: the score CTA's stages no longer hold Q (remote arrival)
+  uint64_t p_full[kPSlots];   // value: P(j) and the max of tile j arrived
+  uint64_t p_free[kPSlots];   // both (multicast commit of PV(j)); the score CTA waits on it
+  uint64_t p_ok[kPSlots];     // value: max checked, O rescaled if needed (4 warps)
+  uint64_t pv_done[kPSlots];  // value: PV(j) completes phase j / kPSlots of pv_done[j % kPSlots]
+  uint64_t o_final;           // value: last PV complete
+  uint64_t fin_l;             // value: 1/l of every head arrived from the score CTA
+  uint64_t fin[1 + 2 * kSBuf];  // each issuing warp's MMAs complete
+  uint32_t mask[kStages];     // valid rows of the tile in each stage
+  uint32_t smask[kSBuf];      // score: valid rows of the tile in each S slot
   uint32_t tmem;
   int32_t abort;
 };
 
 constexpr int kOffStages = 0;
-constexpr int kOffXin = kStages * kStageBytes;
-constexpr int kOffXout = kOffXin + kSBuf * kXBytes;
-constexpr int kOffBars = kOffXout + kSBuf * kXBytes;
+constexpr int kOffP = kStages * kStageBytes;             // value: P slots; score: P staging
+constexpr int kOffFin = kOffP + kPSlots * kPSlotBytes;   // value: 1/l per head
+constexpr int kOffBars = kOffFin + 512;
 constexpr int kSmemBytes = kOffBars + static_cast<int>(sizeof(Bars)) + 1024;  // + alignment slack
 static_assert(kSmemBytes <= 232448, "exceeds the 227 KB of shared memory per CTA");
-static_assert(kStages % 2 == 0, "the two producer warps own alternate stages");
-
-// How a tile's 32 shard tokens reach shared memory.  R consecutive shard
-// tokens lie in one block.  Layout kinds (Rb rows per box, Cb chunks per box):
-//   0: Rb = 8,  Cb = all: group-major stage (8-row groups nch KB apart,
-//                          chunk stride 1 KB)
-//   1: Rb = 32, Cb = all: chunk-major stage (chunk stride 4 KB, groups 1 KB)
-//   2: Rb = R,  Cb = 1:   chunk-major stage, one box per chunk (an 8-row
-//                          group would split a run of the interleave)
-struct TcParams {
-  int32_t mode_whole_blocks;  // 0: runs of I inside blocks (block_size % (D*I) == 0); 1: I % block_size == 0
-  int32_t rows_per_box;       // R
-  int32_t tok_per_block;      // tokens of one shard in one block (mode 0)
-  int32_t run;                // rows of one interleave run inside a box (I in mode 0, 1 in mode 1)
-  int32_t kind;               // layout kind above
-  int32_t box_rows;           // Rb
-};
+static_assert(kPSlotBytes % 1024 == 0 && kOffP % 1024 == 0, "P tiles must sit on swizzle-atom boundaries");
 
 __device__ __forceinline__ void report(int32_t* dev_error, uint32_t bits) {
   if (dev_error) atomicOr(dev_error, static_cast<int32_t>(bits));
@@ -109,22 +125,15 @@ __device__ __forceinline__ void set_abort(Bars& bar, int32_t* dev_error) {
   atomicExch(&bar.abort, 1);
 }
 
-__global__ void __launch_bounds__(kThreads, 1)
-decode_tc_kernel(const __grid_constant__ CUtensorMap tm0, const __grid_constant__ CUtensorMap tm1,
-                 DecodeArgs a, TcParams tp) {
+__global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(DecodeArgs a) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                          ~static_cast<uintptr_t>(1023));
   Bars& bar = *reinterpret_cast<Bars*>(smem + kOffBars);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t cta = cluster_ctarank();
+  const bool score = cta == 0;
   const uint32_t peer = cta ^ 1u;
-  const int nch = 4 + static_cast<int>(cta);     // chunks this CTA owns
-  const int chunk0 = 4 * static_cast<int>(cta);  // first of them
-  // stage layout of this CTA (see TcParams)
-  const int chunk_stride = tp.kind == 0 ? 1024 : kChunkBytes;
-  const int group_stride = tp.kind == 0 ? 1024 * nch : 1024;
-  const CUtensorMap* tmap = cta == 0 ? &tm0 : &tm1;
 
   const int64_t unit = blockIdx.x >> 1;
   const int per_row = a.D * a.plan.splits;
@@ -145,9 +154,12 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm0, const __grid_constant_
     if (warp < 4) {
       const int h = threadIdx.x;
       if (h < a.H) {
-        float* o = a.O_dst + (pair0 + h) * kLatent + 256 * cta;
-        for (int i = 0; i < 64; ++i) reinterpret_cast<float4*>(o)[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (cta == 0) a.lse_dst[pair0 + h] = -INFINITY;
+        if (score) {
+          a.lse_dst[pair0 + h] = -INFINITY;
+        } else {
+          float4* o = reinterpret_cast<float4*>(a.O_dst + (pair0 + h) * kLatent);
+          for (int i = 0; i < kLatent / 4; ++i) o[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
       }
     }
     return;
@@ -155,269 +167,252 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm0, const __grid_constant_
 
   // ---------------------------------------------------------------- setup
   if (threadIdx.x == 0) {
-    for (int i = 0; i < kStages; ++i) { mbar_init(&bar.kv_full[i], 1); mbar_init(&bar.kv_empty[i], 1); }
-    for (int i = 0; i < kSBuf; ++i) {
-      mbar_init(&bar.s_full[i], 1);
-      mbar_init(&bar.s_free[i], 1);
-      mbar_init(&bar.p_full[i], 4);  // one arrival per softmax warp
-      mbar_init(&bar.xfull[i], 4);
-      mbar_init(&bar.xfree[i], 4);
+    for (int i = 0; i < kStages; ++i) {
+      mbar_init(&bar.kv_loaded[i], kProdThreads);
+      mbar_init(&bar.kv_full[i], 1);
+      mbar_init(&bar.s_done[i], score ? 3 : 2);
+      mbar_init(&bar.v_done[i], score ? 1 : 2);
     }
-    mbar_init(&bar.pv_done[0], 1);
-    mbar_init(&bar.pv_done[1], 1);
+    for (int i = 0; i < kSBuf; ++i) { mbar_init(&bar.s_full[i], 3); mbar_init(&bar.s_free[i], 4); }
+    mbar_init(&bar.q_staged, 256);
+    mbar_init(&bar.q_ready, 8);
+    mbar_init(&bar.q_gone, 1);
+    for (int i = 0; i < kPSlots; ++i) {
+      mbar_init(&bar.p_full[i], 1);
+      mbar_init(&bar.p_free[i], 1);
+      mbar_init(&bar.p_ok[i], 4);
+      mbar_init(&bar.pv_done[i], 1);
+    }
     mbar_init(&bar.o_final, 1);
-    for (int i = 0; i < 1 + kSBuf; ++i) mbar_init(&bar.fin[i], 1);
+    mbar_init(&bar.fin_l, 1);
+    for (int i = 0; i < 1 + 2 * kSBuf; ++i) mbar_init(&bar.fin[i], 1);
     bar.abort = 0;
     fence_mbar_init();
-    // every exchange slot starts free: expect the peer's first partials
-    // (four 4 KB copies per slot, one per peer softmax warp)
-    for (int i = 0; i < kSBuf; ++i)
-      for (int w = 0; w < 4; ++w) mbar_arrive_expect_tx(&bar.xfull[i], kXWarpBytes);
+    if (!score) {
+      // every P slot starts free: expect the first P tile and max column
+      for (int i = 0; i < kPSlots; ++i) mbar_arrive_expect_tx(&bar.p_full[i], kPTx);
+      mbar_arrive_expect_tx(&bar.fin_l, 128 * 4);
+    }
   }
-  if (warp == 4) {
+  if (warp == 10) {
     tmem_alloc(&bar.tmem, kTmemCols);
     tmem_relinquish();
-  }
-  if ((warp == 5 || warp == 9) && lane == 0) tma_prefetch_desc(tmap);
-  // Q_c -> TMEM (softmax warps; thread = head = lane): dim k of the CTA's
-  // chunks goes to column k / 2 (low half = even k)
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tbase = bar.tmem;
-  if (warp < 4) {
-    const int h = threadIdx.x;
-    const uint32_t lane_addr = tbase + (static_cast<uint32_t>(warp * 32) << 16);
-    const uint4* qrow = reinterpret_cast<const uint4*>(a.q + static_cast<int64_t>(r) * a.q_stride_tok +
-                                                       static_cast<int64_t>(h < a.H ? h : 0) * kKDim);
-    for (int i = 0; i < nch; ++i) {
-      uint32_t v[32];
-#pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        uint4 x = h < a.H ? __ldg(qrow + (chunk0 + i) * 8 + k) : make_uint4(0u, 0u, 0u, 0u);
-        v[4 * k] = x.x; v[4 * k + 1] = x.y; v[4 * k + 2] = x.z; v[4 * k + 3] = x.w;
-      }
-      tmem_st32(lane_addr + kColQ + 32 * i, v);
-    }
-    tmem_wait_st();
   }
   tc_fence_before();
   __syncthreads();
   cluster_sync();  // peer's barriers initialised and armed before any remote operation
   tc_fence_after();
+  const uint32_t tbase = bar.tmem;
+  if (score && warp < 8) {
+    // Q -> TMEM.  The 147 KB of Q (128 heads x 576 dims, the same for every
+    // unit of a row) come in with one round of cp.async into stages 0-3
+    // (unused until Q is in TMEM): head h at 1152 h, its 16-byte unit u at
+    // position u ^ (h & 7) within each 8-unit group.  Then thread = head =
+    // lane of the warp's lane quarter moves its row to TMEM (warps 0-3 the
+    // even chunks, 4-7 the odd ones): dim k goes to column k / 2 (low half =
+    // even k).  Heads h >= H are zero.
+    const unsigned char* qb = reinterpret_cast<const unsigned char*>(a.q + static_cast<int64_t>(r) * a.q_stride_tok);
+    const uint32_t qs = smem_u32(smem) + kOffStages;
+    for (int p = threadIdx.x; p < 128 * 72; p += 256) {
+      const int hh = p / 72, u = p - hh * 72;
+      const int us = (u & ~7) | ((u & 7) ^ (hh & 7));
+      cp_async16_zfill(qs + hh * 1152 + us * 16, qb + (hh < a.H ? hh : 0) * 1152 + u * 16, hh < a.H ? 16u : 0u);
+    }
+    cp_async_commit();
+    cp_async_wait<0>();
+    mbar_arrive(&bar.q_staged);
+    const bool staged = __all_sync(0xffffffffu, mbar_wait(&bar.q_staged, 0));
+    const int h = (warp & 3) * 32 + lane;
+    const uint32_t lane_addr = tbase + (static_cast<uint32_t>((warp & 3) * 32) << 16);
+    if (staged) {
+      for (int c = warp >> 2; c < kNch; c += 2) {
+        uint32_t v[32];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {  // unit k of the chunk sits at position k ^ (h & 7)
+          const uint4 x = *reinterpret_cast<const uint4*>(smem + kOffStages + h * 1152 + (c * 8 + (k ^ (h & 7))) * 16);
+          v[4 * k] = x.x; v[4 * k + 1] = x.y; v[4 * k + 2] = x.z; v[4 * k + 3] = x.w;
+        }
+        tmem_st32(lane_addr + kColQ + 32 * c, v);
+      }
+    } else {
+      set_abort(bar, a.dev_error);
+    }
+    tmem_wait_st();
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&bar.q_ready);
+  }
 
   const int32_t* trow = a.block_table + static_cast<int64_t>(ri.b) * a.bt_stride;
   const uint32_t smem_base = smem_u32(smem);
-  int xdone = 0;  // softmax: exchange tiles received from the peer
+  int pdone = 0;  // value, warps 0-3: P tiles received
 
-  if (warp == 5 || warp == 9) {
+  if (warp >= kProdWarp0) {
     // ----------------------------------------------------------- producers
-    // Two warps (tiles j = p mod 2, hence disjoint stages, since kStages is
-    // even): TMA issue occupies the issuing thread, so two issue in
-    // parallel.  Per warp, the block ids of its own boxes g = 32k + lane are
-    // fetched one batch ahead (a tile's boxes never straddle batches: 32 %
-    // nbox == 0); lanes issue the tile's TMA boxes.
-    const int p = warp == 5 ? 0 : 1;
-    const int R = tp.rows_per_box;
-    const int nbox = kTile / R;
-    const int runs = a.I / a.block_size;  // mode 1: blocks per run
-    const int32_t dsel = tp.mode_whole_blocks ? 0 : d * a.I;  // first row of shard d in a run group
-    const int Rb = tp.box_rows, nsub = kTile / Rb, npc = tp.kind == 2 ? nch : 1;
-    auto box_k = [&](int32_t l0) -> int32_t {
-      return tp.mode_whole_blocks ? l0 % a.block_size : (l0 % tp.tok_per_block) / a.I;
+    // The 256 threads copy the 16-byte units of the CTA's own chunks of the
+    // tile's rows (upr units per row: chunks 0-3 + 8 = 40 for the score
+    // CTA, chunks 4-7 = 32 for the value CTA); unit p = i * 256 + t, so
+    // consecutive lanes read consecutive bytes of a row.  Lane i of each
+    // warp resolves row i of the tile (shard token -> cache row).  Each
+    // thread's copies of a tile arrive on kv_loaded by themselves when they
+    // complete; the consumers fence them into the async proxy.
+    const int t = threadIdx.x - 32 * kProdWarp0;
+    const int upr = score ? 40 : 32;
+    const int per_thread = kTile * upr / kProdThreads;
+    const unsigned char* kvb = reinterpret_cast<const unsigned char*>(a.kv);
+    uint64_t* own_free = score ? bar.s_done : bar.v_done;
+    // lane i resolves row i of a tile one tile ahead (the block-table load
+    // is consumed an iteration later, so its latency stays off the copies)
+    bool in_n = false;
+    int32_t pos_n = 0, blk_n = -1;
+    auto fetch = [&](int jj) {
+      const int32_t l = lo + jj * kTile + lane;
+      in_n = l < hi;
+      pos_n = in_n ? static_cast<int32_t>(local_to_global(l, d, a.D, a.I)) : 0;
+      blk_n = in_n ? __ldg(trow + pos_n / a.block_size) : -1;
     };
-    auto fetch = [&](int k) -> int32_t {  // -2: past the split, -1: bad block id
-      const int g = 32 * k + lane;                            // this warp's box g
-      const int jj = p + 2 * (g / nbox);                      // its tile
-      const int32_t l0 = lo + (jj * nbox + g % nbox) * R;     // its first shard token
-      if (l0 >= hi) return -2;
-      int32_t lblk;
-      if (tp.mode_whole_blocks) {
-        const int32_t lb = l0 / a.block_size;
-        lblk = (lb / runs) * (a.D * runs) + d * runs + lb % runs;
-      } else {
-        lblk = l0 / tp.tok_per_block;
-      }
-      const int32_t blk = __ldg(trow + lblk);
-      return (blk < 0 || blk >= a.num_blocks) ? -1 : blk;
-    };
-    int32_t cur = fetch(0), nxt = fetch(1);
-    int kcur = 0;
-    int last[kStages];
-    for (int i = 0; i < kStages; ++i) last[i] = -1;
-    for (int m = 0; p + 2 * m < ntiles; ++m) {
-      const int j = p + 2 * m;
+    fetch(0);
+    bool ok = true;
+    if (score) ok = __all_sync(0xffffffffu, mbar_wait(&bar.q_ready, 0));
+    for (int j = 0; j < ntiles && ok; ++j) {
+      const bool in = in_n;
+      const int32_t pos = pos_n, blk = blk_n;
+      if (j + 1 < ntiles) fetch(j + 1);
       const int st = j % kStages;
-      bool ok = lane == 0 ? mbar_wait(&bar.kv_empty[st], ((j / kStages) & 1) ^ 1) : true;
-      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-      if (!ok) { if (lane == 0) set_abort(bar, a.dev_error); break; }
-      if (__any_sync(0xffffffffu, aborted(bar))) break;
-      const int g0 = m * nbox;  // this warp's first box of the tile
-      if ((g0 >> 5) != kcur) { cur = nxt; ++kcur; nxt = fetch(kcur + 1); }
-      // lane bx < nbox owns R-row box bx of this tile
-      const int32_t blk = __shfl_sync(0xffffffffu, cur, (g0 + lane) & 31);
-      const bool mine = lane < nbox;
-      const int32_t l0 = lo + (j * nbox + lane) * R;
-      if (mine && blk == -1) report(a.dev_error, DCP_DEVERR_BAD_BLOCK);
-      const bool valid = mine && blk >= 0;
-      const int nvalid = valid ? min(R, hi - l0) : 0;
-      const uint32_t bits = valid ? ((nvalid >= 32 ? 0xffffffffu : ((1u << nvalid) - 1u)) << (lane * R)) : 0u;
-      const uint32_t mask = __reduce_or_sync(0xffffffffu, bits);
-      const int loaded = __popc(__ballot_sync(0xffffffffu, valid));
-      if (lane == 0) {
-        bar.mask[st] = mask;
-        mbar_arrive_expect_tx(&bar.kv_full[st], static_cast<uint32_t>(loaded * R * nch * 128));
+      ok = __all_sync(0xffffffffu, mbar_wait(&own_free[st], ((j / kStages) & 1) ^ 1));
+      if (ok) ok = !__any_sync(0xffffffffu, aborted(bar));
+      if (!ok) break;
+      const bool valid = in && blk >= 0 && blk < a.num_blocks;
+      if (in && !valid && score && warp == kProdWarp0) report(a.dev_error, DCP_DEVERR_BAD_BLOCK);
+      const int64_t roff =
+          valid ? (static_cast<int64_t>(blk) * a.block_size + pos % a.block_size) * (kKDim * 2) : 0;
+      const uint32_t mask = __ballot_sync(0xffffffffu, valid);
+      if (warp == kProdWarp0 && lane == 0) bar.mask[st] = mask;
+      const uint32_t sbase = smem_base + kOffStages + st * kStageBytes;
+#pragma unroll 5
+      for (int i = 0; i < per_thread; ++i) {
+        const int p = i * kProdThreads + t;
+        const int row = score ? p / 40 : p >> 5;
+        const int u = p - row * upr;
+        const int c = score ? (u < 32 ? (u >> 3) : 8) : 4 + (u >> 3);  // chunk
+        const int64_t ro = __shfl_sync(0xffffffffu, roff, row);
+        const uint32_t dst = sbase + c * kChunkBytes + row * 128 + (((u & 7) ^ (row & 7)) << 4);
+        cp_async16_zfill(dst, kvb + ro + c * 128 + (u & 7) * 16, ((mask >> row) & 1u) ? 16u : 0u);
       }
-      last[st] = j;
-      __syncwarp();
-      unsigned char* sbuf = smem + kOffStages + st * kStageBytes;
-      // (sub-box, piece) pairs q = lane, lane + 32
-      for (int q0 = 0; q0 < nsub * npc; q0 += 32) {
-        const int q = q0 + lane;
-        const int sb = (q / npc) & 7, piece = q % npc;
-        const int bx = (sb * Rb) / R;  // the R-row box (block) holding this sub-box
-        const int32_t b_blk = __shfl_sync(0xffffffffu, blk, bx);
-        const bool b_valid = __shfl_sync(0xffffffffu, valid ? 1 : 0, bx) != 0;
-        if (q < nsub * npc && b_valid) {
-          const int32_t kc = box_k(lo + (j * nbox + bx) * R) + ((sb * Rb) % R) / tp.run;
-          unsigned char* dst = tp.kind == 0 ? sbuf + sb * group_stride
-                             : tp.kind == 1 ? sbuf
-                                            : sbuf + piece * kChunkBytes + sb * Rb * 128;
-          tma_load_5d(dst, tmap, &bar.kv_full[st], 0, dsel, kc, chunk0 + piece, b_blk);
-        }
-      }
+      cp_async_mbar_arrive_noinc(&bar.kv_loaded[st]);
     }
-    // every load this CTA issued has landed before its shared memory goes away
-    if (lane == 0)
-      for (int i = 0; i < kStages; ++i)
-        if (last[i] >= 0) mbar_wait(&bar.kv_full[i], (last[i] / kStages) & 1);
-  } else if (warp >= 6) {
+    if (!ok) set_abort(bar, a.dev_error);
+    cp_async_wait<0>();
+  } else if ((score && warp == 10) || (!score && warp == 8)) {
+    // ---------------------------------------------------------- forwarder
+    // Once this CTA's own rows of tile j have landed: arm kv_full for the
+    // peer's 16 KB, and when the peer's stage is free, copy the 4 chunks the
+    // peer needs into it (score -> value: chunks 0-3; value -> score: 4-7).
+    const uint32_t off = score ? 0u : static_cast<uint32_t>(kFwdBytes);
+    uint64_t* peer_free = score ? bar.v_done : bar.s_done;
+    // the score CTA's stages hold Q until it is in TMEM: the value CTA's
+    // forwards wait for word of that
+    bool ok = __all_sync(0xffffffffu, score ? mbar_wait(&bar.q_ready, 0) : mbar_wait_cluster(&bar.q_gone, 0));
+    if (ok && score && lane == 0) mbar_arrive_remote(map_peer(smem_u32(&bar.q_gone), peer));
+    for (int j = 0; j < ntiles && ok; ++j) {
+      const int st = j % kStages;
+      ok = __all_sync(0xffffffffu, mbar_wait(&bar.kv_loaded[st], (j / kStages) & 1));
+      if (!ok) break;
+      fence_proxy_async_smem();  // the producers' cp.async writes -> the bulk copy and the MMAs
+      if (lane == 0) mbar_arrive_expect_tx(&bar.kv_full[st], kFwdBytes);
+      ok = __all_sync(0xffffffffu, mbar_wait_cluster(&peer_free[st], ((j / kStages) & 1) ^ 1));
+      if (!ok) break;
+      if (lane == 0) {
+        const uint32_t src = smem_base + kOffStages + st * kStageBytes + off;
+        bulk_copy_to_peer(map_peer(src, peer), smem + kOffStages + st * kStageBytes + off, kFwdBytes,
+                          map_peer(smem_u32(&bar.kv_full[st]), peer));
+      }
+      __syncwarp();
+    }
+    if (!ok) set_abort(bar, a.dev_error);
+  } else if (!score && warp == 9) {
+    // ---------------------------------------------------------------- acks
+    // Tell the score CTA when its chunks 0-3 of tile j have landed here, so
+    // that it may reuse the stage they were copied from.
+    bool ok = true;
+    for (int j = 0; j < ntiles && ok; ++j) {
+      const int st = j % kStages;
+      ok = __all_sync(0xffffffffu, mbar_wait_cluster(&bar.kv_full[st], (j / kStages) & 1));
+      if (ok && lane == 0) mbar_arrive_remote(map_peer(smem_u32(&bar.s_done[st]), peer));
+      __syncwarp();
+    }
+    if (!ok) set_abort(bar, a.dev_error);
+  } else if (score && warp >= 4 && warp < 10) {
     // ------------------------------------------------------- S MMA issuers
-    // warp 6+i owns S buffer i and tiles j = i (mod 3)
-    const int b = warp - 6;
+    // warp 4 + 2b + half owns half `half` of S slot b (dims [288 half,
+    // 288 half + 288): 18 k-steps) for tiles j = b (mod 3).  Stage layout:
+    // chunk-major, 4 KB per 64-dim chunk, 8-row groups 1 KB apart.
+    const int b = (warp - 4) >> 1, half = (warp - 4) & 1;
     const uint32_t id_s = idesc_bf16(128, kTile, 0, 0);
-    const uint64_t dk = smem_desc(smem_base + kOffStages, 16, group_stride, kSwizzle128B);
-    const uint32_t dS = tbase + kColS + 32 * b;
-    const int ksteps = 4 * nch;
-    bool ok = true;
-    for (int j = b; j < ntiles; j += kSBuf) {
+    const uint64_t dk = smem_desc(smem_base + kOffStages, 16, 1024, kSwizzle128B);
+    const uint32_t dS = tbase + kColS + 64 * b + 32 * half;
+    bool ok = __all_sync(0xffffffffu, mbar_wait(&bar.q_ready, 0));
+    tc_fence_after();
+    for (int j = b; ok && j < ntiles; j += kSBuf) {
       const int st = j % kStages, u = j / kSBuf;
-      ok = __all_sync(0xffffffffu, mbar_wait(&bar.kv_full[st], (j / kStages) & 1) &&
-                                       mbar_wait(&bar.s_free[b], (u & 1) ^ 1));
+      // s_free first: once the softmax has read S(j - 3) it has read every
+      // earlier tile, so the stage's previous fill (tile j - 5) is consumed
+      // and the kv_full parity below can only mean tile j
+      ok = __all_sync(0xffffffffu, mbar_wait(&bar.s_free[b], (u & 1) ^ 1) &&
+                                       mbar_wait_cluster(&bar.kv_full[st], (j / kStages) & 1));
       if (!ok) break;
-      const uint32_t mask = bar.mask[st];
-      if (mask != 0xffffffffu) {
-        // rows not loaded (tail, bad block): zero them so that P = 0 never
-        // meets a NaN/Inf value row
-        unsigned char* sbuf = smem + kOffStages + st * kStageBytes;
-        for (int row = 0; row < kTile; ++row) {
-          if (mask & (1u << row)) continue;
-          for (int i = 0; i < nch; ++i)
-            reinterpret_cast<uint32_t*>(sbuf + i * chunk_stride + (row >> 3) * group_stride + (row & 7) * 128)[lane] =
-                0u;
+      // the value CTA's chunks 4-7 of tile j have landed: its stage may refill
+      if (half == 1 && lane == 0) mbar_arrive_remote(map_peer(smem_u32(&bar.v_done[st]), peer));
+      // rows that were not loaded are zero and only reach S columns the
+      // softmax masks; the stage's mask travels with the S slot, since the
+      // stage itself is refilled as soon as both halves of S are done
+      if (half == 0 && lane == 0) {
+        bar.smask[b] = bar.mask[st];
+        mbar_arrive(&bar.s_full[b]);
+      }
+      fence_proxy_async_smem();
+      tc_fence_after();
+      if (lane == 0) {
+        const uint64_t so = static_cast<uint64_t>((st * kStageBytes) >> 4);
+#pragma unroll 6
+        for (int i = 0; i < 18; ++i) {
+          const int k = 18 * half + i;
+          mma_ts(dS, tbase + kColQ + 8 * k, dk + so + (((k >> 2) * kChunkBytes + (k & 3) * 32) >> 4), id_s, i > 0);
         }
-        fence_proxy_async_smem();
-        __syncwarp();
-      }
-      tc_fence_after();
-      if (lane == 0) {
-        const uint64_t so = static_cast<uint64_t>((st * kStageBytes) >> 4);
-        for (int k = 0; k < ksteps; ++k)
-          mma_ts(dS, tbase + kColQ + 8 * k, dk + so + (((k >> 2) * chunk_stride + (k & 3) * 32) >> 4), id_s, k > 0);
         mma_commit(&bar.s_full[b]);
+        mma_commit_mc(&bar.s_done[st], 0x3);
       }
       __syncwarp();
     }
     if (!ok) set_abort(bar, a.dev_error);
-    if (lane == 0) mma_commit(&bar.fin[1 + b]);
+    if (lane == 0) mma_commit(&bar.fin[1 + 2 * b + half]);
     __syncwarp();
-    mbar_wait(&bar.fin[1 + b], 0);
-  } else if (warp == 4) {
-    // -------------------------------------------------------- PV MMA issuer
-    // O accumulates across tiles, so PV(j) is issued in order by one thread.
-    // V_c (the CTA's first four chunks) is the MN-major B operand: N (value
-    // dims) atoms = chunks, K (tokens) in 8-row groups.
-    const uint32_t id_o = idesc_bf16(128, 256, 0, 1);
-    const uint64_t dv = smem_desc(smem_base + kOffStages, chunk_stride, group_stride, kSwizzle128B);
-    bool ok = true;
-    for (int jp = 0; jp < ntiles; ++jp) {
-      const int st = jp % kStages, b = jp % kSBuf;
-      ok = __all_sync(0xffffffffu, mbar_wait(&bar.p_full[b], (jp / kSBuf) & 1));
-      if (!ok) break;
-      tc_fence_after();
-      if (lane == 0) {
-        const uint64_t so = static_cast<uint64_t>((st * kStageBytes) >> 4);
-#pragma unroll
-        for (int k = 0; k < 2; ++k)
-          mma_ts(tbase + kColO, tbase + kColS + 32 * b + 8 * k, dv + so + ((2 * group_stride * k) >> 4), id_o,
-                 (jp > 0 || k > 0) ? 1u : 0u);
-        mma_commit(&bar.kv_empty[st]);
-        mma_commit(&bar.s_free[b]);
-        mma_commit(&bar.pv_done[jp & 1]);
-        if (jp == ntiles - 1) mma_commit(&bar.o_final);
-      }
-      __syncwarp();
-    }
-    if (!ok) set_abort(bar, a.dev_error);
-    // all issued MMAs complete before TMEM is released
-    if (lane == 0) mma_commit(&bar.fin[0]);
-    __syncwarp();
-    mbar_wait(&bar.fin[0], 0);
-  } else {
+    mbar_wait(&bar.fin[1 + 2 * b + half], 0);
+  } else if (score && warp < 4) {
     // ------------------------------------------------------------- softmax
-    // Software-pipelined: the partial S of tile j+1 is shipped to the peer
-    // before tile j's softmax, so the exchange latency hides behind a tile.
     const int h = threadIdx.x;
     const uint32_t lane_addr = tbase + (static_cast<uint32_t>(warp * 32) << 16);
     const float sl2 = a.scale * kLog2e;
     float m_used = -INFINITY, l_sum = 0.f;
-    const unsigned char* xin = smem + kOffXin;
-    unsigned char* xout = smem + kOffXout;
-    const int sw = h & 7;
+    const int sw = (h >> 1) & 3;  // 64-byte swizzle of row h
+    const uint32_t p_row = static_cast<uint32_t>((h >> 3) * 512 + (h & 7) * 64);
     bool ok = true;
-    // load own partial S(jj) from TMEM and ship it to the peer's slot
-    auto send = [&](int jj, uint32_t (&sr)[32]) -> bool {
-      const int b = jj % kSBuf, u = jj / kSBuf;
-      if (!__all_sync(0xffffffffu, mbar_wait(&bar.s_full[b], u & 1))) return false;
-      tc_fence_after();
-      tmem_ld32(lane_addr + kColS + 32 * b, sr);
-      tmem_wait_ld();
-      // the peer's slot b (and our staging slot b) are free once the peer has
-      // consumed tile jj - kSBuf
-      if (!__all_sync(0xffffffffu, mbar_wait(&bar.xfree[b], (u & 1) ^ 1))) return false;
-      float4* xo = reinterpret_cast<float4*>(xout + b * kXBytes + h * 128);
-#pragma unroll
-      for (int c = 0; c < 8; ++c)
-        xo[c ^ sw] = make_float4(__uint_as_float(sr[4 * c]), __uint_as_float(sr[4 * c + 1]),
-                                 __uint_as_float(sr[4 * c + 2]), __uint_as_float(sr[4 * c + 3]));
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0)
-        bulk_copy_to_peer(map_peer(smem_base + kOffXin + b * kXBytes + warp * kXWarpBytes, peer),
-                          xout + b * kXBytes + warp * kXWarpBytes, kXWarpBytes,
-                          map_peer(smem_u32(&bar.xfull[b]), peer));
-      return true;
-    };
-    uint32_t sr_cur[32], sr_nxt[32];
-    ok = send(0, sr_cur);
-    for (int j = 0; j < ntiles && ok; ++j) {
-      const int b = j % kSBuf, st = j % kStages, u = j / kSBuf;
-      if (j + 1 < ntiles && !send(j + 1, sr_nxt)) { ok = false; break; }
-      ok = __all_sync(0xffffffffu, mbar_wait(&bar.kv_full[st], (j / kStages) & 1) &&
-                                       mbar_wait(&bar.xfull[b], u & 1));
+    for (int j = 0; j < ntiles; ++j) {
+      const int b = j % kSBuf, slot = j % kPSlots;
+      ok = __all_sync(0xffffffffu, mbar_wait(&bar.s_full[b], (j / kSBuf) & 1));
       if (!ok) break;
-      ++xdone;
-      const uint32_t mask = bar.mask[st];
-      const float4* xi = reinterpret_cast<const float4*>(xin + b * kXBytes + h * 128);
+      tc_fence_after();
+      uint32_t sr[32], sr2[32];
+      tmem_ld32(lane_addr + kColS + 64 * b, sr);
+      tmem_ld32(lane_addr + kColS + 64 * b + 32, sr2);
+      const uint32_t mask = *reinterpret_cast<volatile uint32_t*>(&bar.smask[b]);
+      tmem_wait_ld();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bar.s_free[b]);
       float sc[32];
 #pragma unroll
-      for (int c = 0; c < 8; ++c) {
-        const float4 p = xi[c ^ sw];
-        sc[4 * c] = __uint_as_float(sr_cur[4 * c]) + p.x;
-        sc[4 * c + 1] = __uint_as_float(sr_cur[4 * c + 1]) + p.y;
-        sc[4 * c + 2] = __uint_as_float(sr_cur[4 * c + 2]) + p.z;
-        sc[4 * c + 3] = __uint_as_float(sr_cur[4 * c + 3]) + p.w;
-      }
+      for (int i = 0; i < 32; ++i) sc[i] = __uint_as_float(sr[i]) + __uint_as_float(sr2[i]);
       // online softmax (base 2); masked tokens get weight 0 by selection
       if (mask != 0xffffffffu) {
 #pragma unroll
@@ -429,34 +424,13 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm0, const __grid_constant_
       for (int i = 0; i < 8; ++i) mx[i] = fmaxf(fmaxf(sc[4 * i], sc[4 * i + 1]), fmaxf(sc[4 * i + 2], sc[4 * i + 3]));
       const float tmax = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
                                fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))) * sl2;
+      // lazy rescale: the running max only moves when it would grow by more
+      // than 2^8 (the value CTA rescales O by the same factor)
       const bool grow = m_used == -INFINITY ? (tmax != -INFINITY) : (tmax > m_used + kRescaleLog2);
-      float alpha = 1.f;
-      float m_new = m_used;
       if (grow) {
-        m_new = tmax;
-        if (m_used != -INFINITY) alpha = ex2_approx(m_used - m_new);
+        if (m_used != -INFINITY) l_sum *= ex2_approx(m_used - tmax);
+        m_used = tmax;
       }
-      const bool need_rescale = grow && m_used != -INFINITY;
-      if (__any_sync(0xffffffffu, need_rescale)) {
-        // O holds PV(0..j-1): wait for PV(j-1), then scale this warp's rows.
-        // pv_done[(j-1) & 1] sees PV(j-3) (complete: S(j) reused its
-        // buffer), PV(j-1) and PV(j+1) (impossible before P(j)), so the
-        // parity of phase (j-1)/2 is unambiguous.
-        ok = __all_sync(0xffffffffu, mbar_wait(&bar.pv_done[(j - 1) & 1], ((j - 1) >> 1) & 1));
-        if (!ok) break;
-        tc_fence_after();
-        for (int c = 0; c < 8; ++c) {
-          uint32_t o[32];
-          tmem_ld32(lane_addr + kColO + 32 * c, o);
-          tmem_wait_ld();
-#pragma unroll
-          for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-          tmem_st32(lane_addr + kColO + 32 * c, o);
-        }
-        tmem_wait_st();
-      }
-      l_sum *= alpha;
-      m_used = m_new;
       // p = 2^(s * scale * log2e - m); masked (-inf) scores give exactly 0,
       // and nothing is live while m is still -inf
       const float nm = m_used == -INFINITY ? 0.f : -m_used;
@@ -471,31 +445,124 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm0, const __grid_constant_
         pk[i] = *reinterpret_cast<uint32_t*>(&pb);
       }
       l_sum += (ps[0] + ps[1]) + (ps[2] + ps[3]);
-      tmem_st16(lane_addr + kColS + 32 * b, pk);
-      tmem_wait_st();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(&bar.p_full[b]);
-        // this warp has consumed slot b (the values are in registers): expect
-        // its next 4 KB and let the peer refill it
-        mbar_arrive_expect_tx(&bar.xfull[b], kXWarpBytes);
-        mbar_arrive_remote_relaxed(map_peer(smem_u32(&bar.xfree[b]), peer));
-      }
+      // the slot (and this CTA's staging copy of it) is free once PV(j - kPSlots) is done
+      ok = __all_sync(0xffffffffu, mbar_wait_cluster(&bar.p_free[slot], ((j / kPSlots) & 1) ^ 1));
+      if (!ok) break;
+      unsigned char* stg = smem + kOffP + slot * kPSlotBytes;
 #pragma unroll
-      for (int i = 0; i < 32; ++i) sr_cur[i] = sr_nxt[i];
+      for (int c = 0; c < 4; ++c)
+        *reinterpret_cast<uint4*>(stg + p_row + ((c ^ sw) << 4)) =
+            make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+      fence_proxy_async_smem();
+      __syncwarp();
+      const uint32_t peer_slot = map_peer(smem_base + kOffP + slot * kPSlotBytes, peer);
+      const uint32_t peer_full = map_peer(smem_u32(&bar.p_full[slot]), peer);
+      if (lane == 0)
+        bulk_copy_to_peer(peer_slot + warp * kPWarpBytes, stg + warp * kPWarpBytes, kPWarpBytes, peer_full);
+      st_async_peer_b32(peer_slot + kPBytes + 4 * h, __float_as_uint(m_used), peer_full);
     }
-    if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&bar.o_final, 0));
+    if (!ok) {
+      set_abort(bar, a.dev_error);
+    } else {
+      const bool live = l_sum > 0.f;
+      st_async_peer_b32(map_peer(smem_base + kOffFin + 4 * h, peer), __float_as_uint(live ? 1.f / l_sum : 0.f),
+                        map_peer(smem_u32(&bar.fin_l), peer));
+      if (h < a.H) a.lse_dst[pair0 + h] = live ? (m_used + log2f(l_sum)) * kLn2 : -INFINITY;
+    }
+  } else if (!score && warp == 10) {
+    // -------------------------------------------------------- PV MMA issuer
+    // O accumulates across tiles, so PV(j) is issued in order by one thread.
+    // P (K-major, 64-byte swizzle) and V (the stage's chunks 0-7 read
+    // MN-major: N atoms = 4 KB chunks, K = tokens in 8-row groups 1 KB
+    // apart) both come from shared memory.  Rows that were not loaded are
+    // zero, so P = 0 never meets a NaN/Inf value.
+    const uint32_t id_o = idesc_bf16(128, 256, 0, 1);
+    const uint64_t dv = smem_desc(smem_base + kOffStages, kChunkBytes, 1024, kSwizzle128B);
+    const uint64_t dp = smem_desc(smem_base + kOffP, 16, 512, kSwizzle64B);
+    bool ok = true;
+    for (int j = 0; j < ntiles; ++j) {
+      const int st = j % kStages, slot = j % kPSlots;
+      ok = __all_sync(0xffffffffu, mbar_wait(&bar.p_ok[slot], (j / kPSlots) & 1) &&
+                                       mbar_wait_cluster(&bar.p_full[slot], (j / kPSlots) & 1) &&
+                                       mbar_wait_cluster(&bar.kv_full[st], (j / kStages) & 1));
+      if (!ok) break;
+      // the slot's next fill (tile j + kPSlots) cannot start before PV(j)
+      // frees it, i.e. after this arm
+      if (lane == 0) mbar_arrive_expect_tx(&bar.p_full[slot], kPTx);
+      fence_proxy_async_smem();
+      tc_fence_after();
+      if (lane == 0) {
+        const uint64_t so = static_cast<uint64_t>((st * kStageBytes) >> 4);
+        const uint64_t po = static_cast<uint64_t>((slot * kPSlotBytes) >> 4);
+#pragma unroll
+        for (int k = 0; k < 2; ++k)
+#pragma unroll
+          for (int n = 0; n < 2; ++n)
+            mma_ss(tbase + kColO + 256 * n, dp + po + ((32 * k) >> 4),
+                   dv + so + ((4 * n * kChunkBytes + 2048 * k) >> 4), id_o, (j > 0 || k > 0) ? 1u : 0u);
+        mma_commit_mc(&bar.v_done[st], 0x3);
+        mma_commit_mc(&bar.p_free[slot], 0x3);
+        mma_commit(&bar.pv_done[slot]);
+        if (j == ntiles - 1) mma_commit(&bar.o_final);
+      }
+      __syncwarp();
+    }
+    if (!ok) set_abort(bar, a.dev_error);
+    if (lane == 0) mma_commit(&bar.fin[0]);
+    __syncwarp();
+    mbar_wait(&bar.fin[0], 0);
+  } else if (!score && warp < 8) {
+    const int q4 = warp & 3;
+    const int h = q4 * 32 + lane;
+    const uint32_t lane_addr = tbase + (static_cast<uint32_t>(q4 * 32) << 16);
+    bool ok = true;
+    if (warp < 4) {
+      // ----------------------------------------------- max tracking, rescale
+      float m_prev = -INFINITY;
+      for (int j = 0; j < ntiles; ++j) {
+        const int slot = j % kPSlots;
+        ok = __all_sync(0xffffffffu, mbar_wait_cluster(&bar.p_full[slot], (j / kPSlots) & 1));
+        if (!ok) break;
+        ++pdone;
+        const float m_new = *reinterpret_cast<const volatile float*>(smem + kOffP + slot * kPSlotBytes + kPBytes + 4 * h);
+        const bool need = m_new != m_prev && m_prev != -INFINITY;
+        if (__any_sync(0xffffffffu, need)) {
+          // O holds PV(0..j-1): wait for PV(j-1), then scale this warp's rows.
+          // PV(j - 1 - kPSlots) is complete (P(j) needed its slot), and PV(j)
+          // cannot start before this warp's p_ok, so the parity is unambiguous.
+          const int jp = j - 1;
+          ok = __all_sync(0xffffffffu, mbar_wait(&bar.pv_done[jp % kPSlots], (jp / kPSlots) & 1));
+          if (!ok) break;
+          tc_fence_after();
+          const float alpha = need ? ex2_approx(m_prev - m_new) : 1.f;
+          for (int c = 0; c < 16; ++c) {
+            uint32_t o[32];
+            tmem_ld32(lane_addr + kColO + 32 * c, o);
+            tmem_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+            tmem_st32(lane_addr + kColO + 32 * c, o);
+          }
+          tmem_wait_st();
+        }
+        m_prev = m_new;
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bar.p_ok[slot]);
+      }
+    }
+    // ------------------------------------------------------------ epilogue
+    // warps 0-3 write value dims [0, 256), warps 4-7 dims [256, 512)
+    if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&bar.o_final, 0) && mbar_wait_cluster(&bar.fin_l, 0));
     if (ok) ok = !__any_sync(0xffffffffu, aborted(bar));
     if (!ok) {
       set_abort(bar, a.dev_error);
     } else {
       tc_fence_after();
-      const int64_t pair = pair0 + h;
-      const bool live = l_sum > 0.f;
-      const float inv = live ? 1.f / l_sum : 0.f;
-      float* orow = a.O_dst + pair * kLatent + 256 * cta;
-      for (int c = 0; c < 8; ++c) {
+      const float inv = *reinterpret_cast<const volatile float*>(smem + kOffFin + 4 * h);
+      const int c0 = (warp >> 2) * 8;
+      float* orow = a.O_dst + (pair0 + h) * kLatent;
+      for (int c = c0; c < c0 + 8; ++c) {
         uint32_t o[32];
         tmem_ld32(lane_addr + kColO + 32 * c, o);
         tmem_wait_ld();
@@ -507,77 +574,41 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm0, const __grid_constant_
                             __uint_as_float(o[4 * i + 2]) * inv, __uint_as_float(o[4 * i + 3]) * inv);
         }
       }
-      if (h < a.H && cta == 0) a.lse_dst[pair] = live ? (m_used + log2f(l_sum)) * kLn2 : -INFINITY;
     }
   }
 
   // ------------------------------------------------------------- teardown
+  const bool failed = aborted(bar);
   tc_fence_before();
   __syncthreads();
-  if (warp == 4) {
+  cluster_sync();  // the peer has issued everything it will send here
+  if (failed && !score && threadIdx.x == 0) {
+    // a failed unit may have left some of the score CTA's copies in flight
+    // into the P slots: give each slot's next phase a short bounded wait
+    for (int b = 0; b < kPSlots; ++b) {
+      const int received = pdone > b ? (pdone - 1 - b) / kPSlots + 1 : 0;
+      mbar_wait_cluster(&bar.p_full[b], received & 1, 1u << 16);
+    }
+  }
+  if (warp == 10) {
     tc_fence_after();
     tmem_dealloc(tbase, kTmemCols);
   }
-  const bool failed = aborted(bar);
-  __syncthreads();
-  cluster_sync();  // the peer has issued everything it will send here
-  if (failed && threadIdx.x == 0) {
-    // a failed unit may have left some of the peer's copies in flight into
-    // its slots: give each slot's next phase a short bounded wait
-    for (int b = 0; b < kSBuf; ++b) {
-      const int received = xdone > b ? (xdone - 1 - b) / kSBuf + 1 : 0;
-      mbar_wait_cluster(&bar.xfull[b], received & 1, 1u << 16);
-    }
-  }
 }
 
-// ---------------------------------------------------------------------------
-// host side
-// ---------------------------------------------------------------------------
-typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
-                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
-                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_fn() {
-  static EncodeTiledFn fn = nullptr;
-  if (!fn) {
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeTiledFn>(p);
-  }
-  return fn;
-}
-
-bool tc_params(const DecodeArgs& a, TcParams& tp) {
-  if (a.H > 128) return false;
-  const int bs = a.block_size, D = a.D, I = a.I;
-  if (I % bs == 0) {
-    tp.mode_whole_blocks = 1;
-    tp.rows_per_box = bs < kTile ? bs : kTile;
-    tp.tok_per_block = bs;
-    tp.run = 1;
-  } else if (bs % (D * I) == 0) {
-    const int tpb = bs / D;
-    tp.mode_whole_blocks = 0;
-    tp.rows_per_box = tpb < kTile ? tpb : kTile;
-    tp.tok_per_block = tpb;
-    tp.run = I;
-  } else {
-    return false;
-  }
-  const int R = tp.rows_per_box;
-  if (R < 4 || kTile % R || tp.tok_per_block % R || R % tp.run) return false;
-  if (R == 32) {
-    tp.kind = 1; tp.box_rows = 32;
-  } else if (R >= 8 && 8 % tp.run == 0) {
-    tp.kind = 0; tp.box_rows = 8;
-  } else {
-    tp.kind = 2; tp.box_rows = R;
-  }
-  return true;
+cudaLaunchConfig_t launch_config(int64_t units, cudaStream_t st, cudaLaunchAttribute* attr) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(2 * units));
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.stream = st;
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cfg;
 }
 
 }  // namespace
@@ -591,17 +622,8 @@ int decode_tc_resident_ctas() {
   if (dev == cached_dev) return cached;
   if (cudaFuncSetAttribute(decode_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) !=
       cudaSuccess) { cudaGetLastError(); return 0; }
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(2);
-  cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = kSmemBytes;
   cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 2;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cudaLaunchConfig_t cfg = launch_config(1, nullptr, attr);
   int clusters = 0;
   if (cudaOccupancyMaxActiveClusters(&clusters, decode_tc_kernel, &cfg) != cudaSuccess || clusters <= 0) {
     cudaGetLastError();
@@ -612,60 +634,17 @@ int decode_tc_resident_ctas() {
   return cached;
 }
 
-bool decode_tc_supported(const DecodeArgs& a) {
-  TcParams tp;
-  return tc_params(a, tp) && (a.plan.chunk % kTile) == 0;
-}
+bool decode_tc_supported(const DecodeArgs& a) { return a.H <= 128 && (a.plan.chunk % kTile) == 0; }
 
 cudaError_t launch_decode_tc(const DecodeArgs& a, cudaStream_t st) {
-  TcParams tp;
-  if (!tc_params(a, tp)) return cudaErrorInvalidValue;
-  EncodeTiledFn enc = encode_fn();
-  if (!enc) return cudaErrorNotSupported;
-  // 5-D view of the cache: [64 elements of a chunk][rows of a run group]
-  // [run groups of a block][9 chunks][blocks].  Mode 0: a run group is the
-  // D*I rows that hold one run of every shard; mode 1: one group of
-  // block_size rows.  The chunk dimension (stride 128 B) comes after the row
-  // dimensions, so one box can carry several chunks of the same rows: CTA 0
-  // boxes carry chunks 0-3, CTA 1 boxes chunks 4-8 (kind 2: one chunk).
-  const int bs = a.block_size;
-  const cuuint64_t DI = tp.mode_whole_blocks ? 1 : static_cast<cuuint64_t>(a.D) * a.I;
-  const cuuint64_t groups = tp.mode_whole_blocks ? static_cast<cuuint64_t>(bs) : bs / DI;
-  const cuuint64_t row = kKDim * 2;
-  cuuint64_t dims[5] = {64, DI, groups, 9, static_cast<cuuint64_t>(a.num_blocks)};
-  cuuint64_t strides[4] = {row, tp.mode_whole_blocks ? row : row * DI, 128, row * bs};
-  cuuint32_t box[5] = {64, static_cast<cuuint32_t>(tp.run), static_cast<cuuint32_t>(tp.box_rows / tp.run), 1, 1};
-  cuuint32_t es[5] = {1, 1, 1, 1, 1};
-  CUtensorMap m0, m1;
-  void* base = const_cast<__nv_bfloat16*>(a.kv);
-  box[3] = tp.kind == 2 ? 1 : 4;
-  if (enc(&m0, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, base, dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
-          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) !=
-      CUDA_SUCCESS)
-    return cudaErrorInvalidValue;
-  box[3] = tp.kind == 2 ? 1 : 5;
-  if (enc(&m1, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, base, dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
-          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) !=
-      CUDA_SUCCESS)
-    return cudaErrorInvalidValue;
-
+  if (!decode_tc_supported(a)) return cudaErrorInvalidValue;
   cudaError_t e = cudaFuncSetAttribute(decode_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   if (e != cudaSuccess) return e;
   const int64_t units = static_cast<int64_t>(a.T) * a.D * a.plan.splits;
   if (2 * units > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(2 * units));
-  cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = kSmemBytes;
-  cfg.stream = st;
   cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 2;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, decode_tc_kernel, m0, m1, a, tp);
+  cudaLaunchConfig_t cfg = launch_config(units, st, attr);
+  return cudaLaunchKernelEx(&cfg, decode_tc_kernel, a);
 }
 
 }  // namespace dcp

@@ -163,6 +163,19 @@ __device__ __forceinline__ void tma_load_5d(void* dst, const void* tmap, uint64_
       : "memory");
 }
 
+// Multicast form of tma_load_5d: the box lands at the same shared-memory
+// offset in every CTA of the cluster named in `cta_mask`, and each of them
+// gets the tx bytes on its mbarrier at the offset of `bar`.
+__device__ __forceinline__ void tma_load_5d_mc(void* dst, const void* tmap, uint64_t* bar, int32_t c0, int32_t c1,
+                                               int32_t c2, int32_t c3, int32_t c4, uint16_t cta_mask) {
+  asm volatile(
+      "cp.async.bulk.tensor.5d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster"
+      " [%0], [%1, {%3, %4, %5, %6, %7}], [%2], %8;" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4),
+      "h"(cta_mask)
+      : "memory");
+}
+
 // Copy `bytes` (multiple of 16) from this CTA's shared memory to the peer's
 // (`dst_peer`, `bar_peer` from map_peer); completes tx bytes on the peer's
 // mbarrier.
@@ -185,9 +198,27 @@ __device__ __forceinline__ void st_async_peer(uint32_t dst_peer, float4 v, uint3
       : "memory");
 }
 
+// 4-byte store into the peer CTA's shared memory that completes 4 tx bytes
+// on the peer's mbarrier `bar_peer`.
+__device__ __forceinline__ void st_async_peer_b32(uint32_t dst_peer, uint32_t v, uint32_t bar_peer) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];" ::"r"(dst_peer), "r"(v),
+               "r"(bar_peer)
+               : "memory");
+}
+
 // 16-byte global -> shared copy through L2 (LSU path, bypasses L1).
 __device__ __forceinline__ void cp_async16(uint32_t dst_smem, const void* src) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst_smem), "l"(src) : "memory");
+}
+// Same, with a source size of 0 or 16 bytes: 0 writes 16 zero bytes and
+// reads nothing (for rows that must not be loaded).
+__device__ __forceinline__ void cp_async16_zfill(uint32_t dst_smem, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst_smem), "l"(src), "r"(src_bytes) : "memory");
+}
+// Arrive on `bar` (without raising its expected count) once every cp.async
+// this thread has issued so far is complete.
+__device__ __forceinline__ void cp_async_mbar_arrive_noinc(uint64_t* bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 template <int N>
@@ -243,6 +274,16 @@ __device__ __forceinline__ void mma_commit(uint64_t* bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
                    smem_u32(bar))
                : "memory");
+}
+
+// Multicast commit: once this thread's tcgen05 ops complete, arrive once on
+// the mbarrier at the offset of `bar` in every CTA named in `cta_mask`.
+__device__ __forceinline__ void mma_commit_mc(uint64_t* bar, uint16_t cta_mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+          smem_u32(bar)),
+      "h"(cta_mask)
+      : "memory");
 }
 
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }

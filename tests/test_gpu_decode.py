@@ -29,6 +29,11 @@ SMALL = [
                   interleave=1),
     wl.DecodeSpec("h128_long_split", seed=38, B=1, seq_lens=(9000,), H=128, block_size=64, D=8,
                   interleave=1),
+    # more units than clusters, so one split per shard: 20-25 tiles per unit
+    # (every stage, S buffer and P slot reused several times)
+    wl.DecodeSpec("h128_b12_unsplit", seed=39, B=12,
+                  seq_lens=(5000, 6100, 5300, 6400, 5700, 5100, 6000, 5500, 6300, 5200, 5900, 6200),
+                  H=128, block_size=64, D=8, interleave=1),
 ]
 
 
