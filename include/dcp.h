@@ -162,8 +162,8 @@ dcp_status_t dcp_mla_decode_partial(
 
 /*
  * LSE-weighted combine of D shard partials, with empty-shard and padding-row
- * masking [north-star formula; PRHUB step 4 "exp2 LSE weighted merge";
- * PR50484 "CUDA-graph padding follow-up"].
+ * masking [PRHUB step 4 "exp2 LSE weighted merge"; PR50484 "CUDA-graph
+ * padding follow-up"].
  *
  * For each row r and head h: a row whose request has seq_lens == 0 (or that
  * lies past qsl[B]) is a padding row: out = 0, out_lse = -inf, nothing else

@@ -1,14 +1,18 @@
-// LSE-weighted combine / split merge: a vectorised, coalesced streaming
-// reduction (no tensor cores; HBM-bound).
+// LSE-weighted combine / split merge: a streaming reduction over nsrc
+// partials (no tensor cores; HBM/L2-bound, and latency-bound when there are
+// few (row, head) pairs).
 //
-// One warp owns one (row, head) pair.  Lane d < nsrc reads source d's LSE;
-// the live set E = {d : lse_d != -inf} is a warp ballot, so the partial
-// output of a masked source is never loaded [spec formula; the
-// "[Kimi-K3] DCP support" summary on prhub.com.cn, implementation step 4:
-// -inf at the source, zero-weight sources skipped by the consumer].
-// Weights are exp2(lse_d * log2 e - M) with M the maximum over E; the 512
-// outputs are spread over the warp as four 16-byte loads per lane and
-// source, so every load instruction reads 512 contiguous bytes.
+// One 128-thread CTA owns one (row, head) pair.  Warp 0 reads the nsrc LSEs
+// (lane d: source d), takes the live set E = {d : lse_d != -inf} as a warp
+// ballot, and publishes the weights exp2(lse_d log2 e - M) (M = max over E;
+// 0 outside E) to shared memory; the partial output of a masked source is
+// never loaded ["[Kimi-K3] DCP support" summary on prhub.com.cn,
+// implementation step 4: -inf at the source, zero-weight sources skipped by
+// the consumer].  Thread t then owns output columns 4t .. 4t+3 and issues
+// the 16-byte loads of up to 8 sources at once, so a pair costs one or two
+// memory round trips instead of one per source.  The kernel waits on the
+// grid it depends on (programmatic dependent launch) only after its launch,
+// so its launch overlaps the tail of the kernel that produced its inputs.
 #include "dcp_kernels.h"
 
 #include <cmath>
@@ -16,7 +20,8 @@
 namespace dcp {
 namespace {
 
-constexpr int kWarpsPerCta = 8;
+constexpr int kThreadsPerPair = kLatent / 4;  // one float4 column each
+constexpr int kBatch = 8;                     // sources loaded per round trip
 constexpr unsigned kFull = 0xffffffffu;
 
 __device__ __forceinline__ float warp_max(float v) {
@@ -41,64 +46,66 @@ __device__ __forceinline__ void store4(__nv_bfloat16* p, float4 v) {
 }
 
 template <typename OutT, bool kRowMask>
-__global__ void __launch_bounds__(kWarpsPerCta * 32)
+__global__ void __launch_bounds__(kThreadsPerPair)
 lse_merge_kernel(const float* __restrict__ O_src, const float* __restrict__ lse_src,
                  int64_t o_stride, int64_t lse_stride, int nsrc, int64_t npairs, int32_t H,
                  const int32_t* __restrict__ seq_lens, const int32_t* __restrict__ qsl, int32_t B,
                  OutT* __restrict__ out, float* out_lse) {
-  const int lane = threadIdx.x & 31;
-  const int64_t pair = static_cast<int64_t>(blockIdx.x) * kWarpsPerCta + (threadIdx.x >> 5);
-  if (pair >= npairs) return;
-  OutT* dst = out + pair * kLatent;
+  __shared__ float w_s[32];
+  __shared__ int32_t live_s[32];
+  __shared__ int32_t nlive_s;
+  __shared__ float inv_s;
+  asm volatile("griddepcontrol.wait;" ::: "memory");  // inputs written by the preceding grid
+  const int t = threadIdx.x, lane = t & 31;
+  const int64_t pair = blockIdx.x;
+  OutT* dst = out + pair * kLatent + 4 * t;
 
-  bool pad = false;
-  if (kRowMask) pad = row_is_padding(seq_lens, qsl, B, static_cast<int32_t>(pair / H));
-  if (!pad) {
-    // out_lse may alias lse_src's source-0 slice: all reads of this pair's
-    // LSEs happen here, before the single write below.
-    const float l = lane < nsrc ? __ldg(lse_src + lane * lse_stride + pair) : -INFINITY;
+  if (t < 32) {
+    bool pad = false;
+    if (kRowMask) pad = row_is_padding(seq_lens, qsl, B, static_cast<int32_t>(pair / H));
+    // out_lse may alias lse_src's source-0 slice: every read of this pair's
+    // LSEs happens here, before the single write below.
+    const float l = !pad && lane < nsrc ? __ldg(lse_src + lane * lse_stride + pair) : -INFINITY;
     const bool live = l != -INFINITY;
-    unsigned live_mask = __ballot_sync(kFull, live);
-    if (live_mask) {
-      const float l2 = live ? l * kLog2e : -INFINITY;
-      const float M = warp_max(l2);
-      const float w = live ? exp2f(l2 - M) : 0.f;
-      const float den = warp_sum(w);
-      float4 acc[4];
-#pragma unroll
-      for (int k = 0; k < 4; ++k) acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
-      while (live_mask) {
-        const int d = __ffs(live_mask) - 1;
-        live_mask &= live_mask - 1;
-        const float wd = __shfl_sync(kFull, w, d);
-        const float4* src = reinterpret_cast<const float4*>(O_src + d * o_stride + pair * kLatent);
-        float4 v[4];
-#pragma unroll
-        for (int k = 0; k < 4; ++k) v[k] = __ldcs(src + lane + 32 * k);  // streamed once
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          acc[k].x = fmaf(wd, v[k].x, acc[k].x);
-          acc[k].y = fmaf(wd, v[k].y, acc[k].y);
-          acc[k].z = fmaf(wd, v[k].z, acc[k].z);
-          acc[k].w = fmaf(wd, v[k].w, acc[k].w);
-        }
-      }
-      const float inv = 1.f / den;
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        float4 o = acc[k];
-        o.x *= inv; o.y *= inv; o.z *= inv; o.w *= inv;
-        store4(dst + 4 * lane + 128 * k, o);
-      }
-      if (lane == 0) out_lse[pair] = (M + log2f(den)) * kLn2;
-      return;
+    const unsigned live_mask = __ballot_sync(kFull, live);
+    const float l2 = live ? l * kLog2e : -INFINITY;
+    const float M = live_mask ? warp_max(l2) : 0.f;
+    const float w = live ? exp2f(l2 - M) : 0.f;
+    const float den = warp_sum(w);
+    if (live) {
+      const int k = __popc(live_mask & ((1u << lane) - 1u));  // rank among the live sources
+      live_s[k] = lane;
+      w_s[k] = w;
+    }
+    if (lane == 0) {
+      nlive_s = __popc(live_mask);
+      inv_s = live_mask ? 1.f / den : 0.f;
+      out_lse[pair] = live_mask ? (M + log2f(den)) * kLn2 : -INFINITY;
     }
   }
-  // padding row, or no live source: zeros and -inf, nothing else read
-  const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+  __syncthreads();
+  const int n = nlive_s;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int k0 = 0; k0 < n; k0 += kBatch) {
+    float4 v[kBatch];
 #pragma unroll
-  for (int k = 0; k < 4; ++k) store4(dst + 4 * lane + 128 * k, z);
-  if (lane == 0) out_lse[pair] = -INFINITY;
+    for (int k = 0; k < kBatch; ++k)
+      if (k0 + k < n)
+        v[k] = __ldcs(reinterpret_cast<const float4*>(O_src + live_s[k0 + k] * o_stride + pair * kLatent) + t);
+#pragma unroll
+    for (int k = 0; k < kBatch; ++k)
+      if (k0 + k < n) {
+        const float wd = w_s[k0 + k];
+        acc.x = fmaf(wd, v[k].x, acc.x);
+        acc.y = fmaf(wd, v[k].y, acc.y);
+        acc.z = fmaf(wd, v[k].z, acc.z);
+        acc.w = fmaf(wd, v[k].w, acc.w);
+      }
+  }
+  // padding row or no live source: n == 0, inv == 0, so zeros
+  const float inv = inv_s;
+  acc.x *= inv; acc.y *= inv; acc.z *= inv; acc.w *= inv;
+  store4(dst, acc);
 }
 
 template <typename OutT, bool kRowMask>
@@ -106,11 +113,18 @@ cudaError_t launch(const float* O_src, const float* lse_src, int64_t o_stride, i
                    int nsrc, int64_t npairs, int32_t H, const int32_t* seq_lens, const int32_t* qsl,
                    int32_t B, OutT* out, float* out_lse, cudaStream_t st) {
   if (npairs <= 0) return cudaSuccess;
-  const int64_t grid = (npairs + kWarpsPerCta - 1) / kWarpsPerCta;
-  if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-  lse_merge_kernel<OutT, kRowMask><<<static_cast<unsigned>(grid), kWarpsPerCta * 32, 0, st>>>(
-      O_src, lse_src, o_stride, lse_stride, nsrc, npairs, H, seq_lens, qsl, B, out, out_lse);
-  return cudaGetLastError();
+  if (npairs > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(npairs));
+  cfg.blockDim = dim3(kThreadsPerPair);
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, lse_merge_kernel<OutT, kRowMask>, O_src, lse_src, o_stride, lse_stride, nsrc,
+                            npairs, H, seq_lens, qsl, B, out, out_lse);
 }
 
 }  // namespace

@@ -19,12 +19,16 @@
 // the other inside the tile loop.
 //
 // Each tile is read from HBM once, half by each CTA: the score CTA loads
-// chunks 0-3 and the rope chunk 8 (20 KB), the value CTA chunks 4-7 (16 KB),
-// with 16-byte cp.async, one shard token per row, straight into the
-// 128B-swizzled chunk-major layout the MMAs read.  Each CTA then forwards the
-// part its peer needs with one 16 KB DSMEM bulk copy (score -> value: chunks
-// 0-3; value -> score: chunks 4-7).  This exchange carries raw latents, so
-// it runs as soon as the rows land and sits on no dependency loop.
+// chunks 0-3 and the rope chunk 8 (20 KB) into its stage ring, the value CTA
+// chunks 4-7 (16 KB) into its "own" ring, with 16-byte cp.async, one shard
+// token per row, straight into the 128B-swizzled chunk-major layout the MMAs
+// read.  Each CTA forwards the 16 KB its peer lacks with one DSMEM bulk copy:
+// value -> score chunks 4-7 (into the stage, which then holds the whole tile
+// for S), score -> value chunks 0-3 (into a 3-slot receive ring; PV reads V
+// from the receive slot and the own slot).  The own ring is 8 deep, so the
+// loop through PV that feeds back into the loads (and through them into S)
+// spans 8 tiles.  A DSMEM copy was measured at ~900 cycles of round trip plus
+// ~47 cycles per KB, so each direction carries at most 24 KB per tile.
 // Row-by-row addressing takes any paging geometry (block size, shard count,
 // interleave); rows that must not be read (past the split, bad block ids)
 // are zero-filled.  (TMA boxes were measured to cost a few hundred cycles
@@ -39,8 +43,10 @@
 //                      half k of S for tiles j = i mod 3 into S slot i (a
 //                      tcgen05.mma holds its issuing thread far longer than
 //                      an N=32 product takes, so issue is spread over warps)
-//               value: 4-7 epilogue columns 256-511; 8 forwarder; 9 acks
-//   warp 10     both:  TMEM allocation; score: forwarder; value: PV issuer
+//               value: 4-7 epilogue columns 256-511; 8 forwarder (own
+//                      ring -> score stage); 9 receive-ring arrivals
+//   warp 10     both:  TMEM allocation; score: forwarder (stage -> receive
+//                      ring); value: PV issuer
 //   warps 11-18 both:  producers (cp.async; the score CTA's wait until Q has
 //                      left stages 0-3 for TMEM)
 // Every wait is bounded (a timeout sets DCP_DEVERR_TIMEOUT and ends the unit).
@@ -56,13 +62,15 @@ namespace {
 using namespace sm100;
 
 constexpr int kTile = 32;                        // tokens per tile (MMA N of S, K of PV)
-constexpr int kStages = 5;                       // stage ring of each CTA
+constexpr int kStages = 5;                       // score CTA: stage ring
 constexpr int kNch = 9;                          // 64-dim chunks of a latent row
 constexpr int kChunkBytes = kTile * 128;         // 32 rows x 64 bf16, 128B-swizzled
 constexpr int kStageBytes = kNch * kChunkBytes;  // 36 KB
 constexpr int kProdWarp0 = 11, kProdWarps = 8;   // producer warps
 constexpr int kProdThreads = 32 * kProdWarps;
-constexpr int kFwdBytes = 4 * kChunkBytes;       // forwarded each way per tile: 4 chunks
+constexpr int kHalfBytes = 4 * kChunkBytes;      // 4 chunks: forwarded each way per tile
+constexpr int kOwn = 8;                          // value CTA: own ring slots (chunks 4-7)
+constexpr int kRecv = 3;                         // value CTA: receive ring slots (chunks 0-3)
 constexpr int kSBuf = 3;                         // S slots (two 32-column halves each) in TMEM
 constexpr int kPSlots = 4;                       // P slots in the value CTA
 constexpr int kPBytes = 128 * kTile * 2;         // P tile: 128 rows x 32 bf16, 64B-swizzled
@@ -79,15 +87,15 @@ constexpr uint32_t kColO = 0;    // value: 512 columns of O
 constexpr uint32_t kTmemCols = 512;
 
 struct __align__(8) Bars {
-  uint64_t kv_loaded[kStages];  // both: this CTA's own rows of tile j landed (every producer thread)
-  uint64_t kv_full[kStages];    // both: own rows (forwarder's arrival) + the peer's 16 KB landed
-  // s_done: score = stage free for own loads (both halves of S(j) + the value
-  //         CTA's ack that chunks 0-3 of tile j landed there); value = the
-  //         score CTA's stage free for the next forward (both halves of S(j))
-  // v_done: value = stage free for own loads (PV(j) + the score CTA's ack
-  //         that chunks 4-7 landed there); score = the value CTA's stage free
-  //         for the next forward (PV(j))
-  uint64_t s_done[kStages], v_done[kStages];
+  uint64_t kv_loaded[kStages];  // score: own rows of tile j landed (every producer thread)
+  uint64_t kv_full[kStages];    // score: the value CTA's 16 KB of tile j landed (armed by a producer)
+  // s_done (both CTAs): the score CTA's stage of tile j is free again: both
+  // halves of S(j) done and tile j's V part has landed in the value CTA
+  uint64_t s_done[kStages];
+  uint64_t own_loaded[kOwn];    // value: rows of tile j in own slot j % kOwn (every producer thread)
+  uint64_t own_free[kOwn];      // value: PV(j) done with own slot j % kOwn
+  uint64_t v_full[kRecv];       // value: chunks 0-3 of tile j landed in receive slot j % kRecv
+  uint64_t v_free[kRecv];       // score (multicast commit of PV(j)): receive slot j % kRecv may refill
   uint64_t s_full[kSBuf];     // score: both halves' commits + the slot's mask
   uint64_t s_free[kSBuf];     // score: the softmax has read the slot (4 warps)
   uint64_t q_staged;          // score: Q is in shared memory (threads of warps 0-7)
@@ -106,13 +114,16 @@ struct __align__(8) Bars {
   int32_t abort;
 };
 
-constexpr int kOffStages = 0;
+constexpr int kOffStages = 0;                            // score: stage ring
+constexpr int kOffOwn = 0;                               // value: own ring
+constexpr int kOffRecv = kOwn * kHalfBytes;              // value: receive ring
 constexpr int kOffP = kStages * kStageBytes;             // value: P slots; score: P staging
 constexpr int kOffFin = kOffP + kPSlots * kPSlotBytes;   // value: 1/l per head
 constexpr int kOffBars = kOffFin + 512;
 constexpr int kSmemBytes = kOffBars + static_cast<int>(sizeof(Bars)) + 1024;  // + alignment slack
 static_assert(kSmemBytes <= 232448, "exceeds the 227 KB of shared memory per CTA");
 static_assert(kPSlotBytes % 1024 == 0 && kOffP % 1024 == 0, "P tiles must sit on swizzle-atom boundaries");
+static_assert(kOffRecv + kRecv * kHalfBytes <= kOffP, "value CTA rings overlap the P slots");
 
 __device__ __forceinline__ void report(int32_t* dev_error, uint32_t bits) {
   if (dev_error) atomicOr(dev_error, static_cast<int32_t>(bits));
@@ -170,9 +181,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(DecodeArgs a) {
     for (int i = 0; i < kStages; ++i) {
       mbar_init(&bar.kv_loaded[i], kProdThreads);
       mbar_init(&bar.kv_full[i], 1);
-      mbar_init(&bar.s_done[i], score ? 3 : 2);
-      mbar_init(&bar.v_done[i], score ? 1 : 2);
+      mbar_init(&bar.s_done[i], 3);
     }
+    for (int i = 0; i < kOwn; ++i) { mbar_init(&bar.own_loaded[i], kProdThreads); mbar_init(&bar.own_free[i], 1); }
+    for (int i = 0; i < kRecv; ++i) { mbar_init(&bar.v_full[i], 1); mbar_init(&bar.v_free[i], 1); }
     for (int i = 0; i < kSBuf; ++i) { mbar_init(&bar.s_full[i], 3); mbar_init(&bar.s_free[i], 4); }
     mbar_init(&bar.q_staged, 256);
     mbar_init(&bar.q_ready, 8);
@@ -191,6 +203,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(DecodeArgs a) {
     if (!score) {
       // every P slot starts free: expect the first P tile and max column
       for (int i = 0; i < kPSlots; ++i) mbar_arrive_expect_tx(&bar.p_full[i], kPTx);
+      for (int i = 0; i < kRecv; ++i) mbar_arrive_expect_tx(&bar.v_full[i], kHalfBytes);
       mbar_arrive_expect_tx(&bar.fin_l, 128 * 4);
     }
   }
@@ -250,8 +263,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(DecodeArgs a) {
   if (warp >= kProdWarp0) {
     // ----------------------------------------------------------- producers
     // The 256 threads copy the 16-byte units of the CTA's own chunks of the
-    // tile's rows (upr units per row: chunks 0-3 + 8 = 40 for the score
-    // CTA, chunks 4-7 = 32 for the value CTA); unit p = i * 256 + t, so
+    // tile's rows (upr units per row: chunks 0-3 + 8 = 40 into the score
+    // CTA's stage, chunks 4-7 = 32 into the value CTA's own slot, laid out
+    // as the stage's chunks 4-7 are); unit p = i * 256 + t, so
     // consecutive lanes read consecutive bytes of a row.  Lane i of each
     // warp resolves row i of the tile (shard token -> cache row).  Each
     // thread's copies of a tile arrive on kv_loaded by themselves when they
@@ -260,7 +274,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(DecodeArgs a) {
     const int upr = score ? 40 : 32;
     const int per_thread = kTile * upr / kProdThreads;
     const unsigned char* kvb = reinterpret_cast<const unsigned char*>(a.kv);
-    uint64_t* own_free = score ? bar.s_done : bar.v_done;
+    uint64_t* own_free = score ? bar.s_done : bar.own_free;
+    uint64_t* own_loaded = score ? bar.kv_loaded : bar.own_loaded;
+    const int nslots = score ? kStages : kOwn;
     // lane i resolves row i of a tile one tile ahead (the block-table load
     // is consumed an iteration later, so its latency stays off the copies)
     bool in_n = false;
@@ -278,8 +294,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(DecodeArgs a) {
       const bool in = in_n;
       const int32_t pos = pos_n, blk = blk_n;
       if (j + 1 < ntiles) fetch(j + 1);
-      const int st = j % kStages;
-      ok = __all_sync(0xffffffffu, mbar_wait(&own_free[st], ((j / kStages) & 1) ^ 1));
+      const int st = j % nslots;
+      ok = __all_sync(0xffffffffu, mbar_wait(&own_free[st], ((j / nslots) & 1) ^ 1));
       if (ok) ok = !__any_sync(0xffffffffu, aborted(bar));
       if (!ok) break;
       const bool valid = in && blk >= 0 && blk < a.num_blocks;
@@ -287,8 +303,15 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(DecodeArgs a) {
       const int64_t roff =
           valid ? (static_cast<int64_t>(blk) * a.block_size + pos % a.block_size) * (kKDim * 2) : 0;
       const uint32_t mask = __ballot_sync(0xffffffffu, valid);
-      if (warp == kProdWarp0 && lane == 0) bar.mask[st] = mask;
-      const uint32_t sbase = smem_base + kOffStages + st * kStageBytes;
+      if (score && warp == kProdWarp0 && lane == 0) {
+        bar.mask[st] = mask;
+        // tile j - 5 is done with the stage, so kv_full's previous phase is
+        // complete: arm it for the value CTA's 16 KB of tile j
+        mbar_arrive_expect_tx(&bar.kv_full[st], kHalfBytes);
+      }
+      // the value CTA's own slot holds chunks 4-7 at chunk offsets 0-3
+      const uint32_t sbase = score ? smem_base + kOffStages + st * kStageBytes
+                                   : smem_base + kOffOwn + st * kHalfBytes - 4 * kChunkBytes;
 #pragma unroll 5
       for (int i = 0; i < per_thread; ++i) {
         const int p = i * kProdThreads + t;
@@ -299,46 +322,60 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(DecodeArgs a) {
         const uint32_t dst = sbase + c * kChunkBytes + row * 128 + (((u & 7) ^ (row & 7)) << 4);
         cp_async16_zfill(dst, kvb + ro + c * 128 + (u & 7) * 16, ((mask >> row) & 1u) ? 16u : 0u);
       }
-      cp_async_mbar_arrive_noinc(&bar.kv_loaded[st]);
+      cp_async_mbar_arrive_noinc(&own_loaded[st]);
     }
     if (!ok) set_abort(bar, a.dev_error);
     cp_async_wait<0>();
-  } else if ((score && warp == 10) || (!score && warp == 8)) {
-    // ---------------------------------------------------------- forwarder
-    // Once this CTA's own rows of tile j have landed: arm kv_full for the
-    // peer's 16 KB, and when the peer's stage is free, copy the 4 chunks the
-    // peer needs into it (score -> value: chunks 0-3; value -> score: 4-7).
-    const uint32_t off = score ? 0u : static_cast<uint32_t>(kFwdBytes);
-    uint64_t* peer_free = score ? bar.v_done : bar.s_done;
-    // the score CTA's stages hold Q until it is in TMEM: the value CTA's
-    // forwards wait for word of that
-    bool ok = __all_sync(0xffffffffu, score ? mbar_wait(&bar.q_ready, 0) : mbar_wait_cluster(&bar.q_gone, 0));
-    if (ok && score && lane == 0) mbar_arrive_remote(map_peer(smem_u32(&bar.q_gone), peer));
+  } else if (score && warp == 10) {
+    // ------------------------------------------------- score CTA forwarder
+    // Once this CTA's own rows of tile j have landed and the value CTA's
+    // receive slot is free, copy chunks 0-3 (16 KB) into it.
+    bool ok = __all_sync(0xffffffffu, mbar_wait(&bar.q_ready, 0));
+    // the value CTA's forwards into the stages (which held Q) may start
+    if (ok && lane == 0) mbar_arrive_remote(map_peer(smem_u32(&bar.q_gone), peer));
     for (int j = 0; j < ntiles && ok; ++j) {
-      const int st = j % kStages;
-      ok = __all_sync(0xffffffffu, mbar_wait(&bar.kv_loaded[st], (j / kStages) & 1));
+      const int st = j % kStages, rs = j % kRecv;
+      ok = __all_sync(0xffffffffu, mbar_wait(&bar.kv_loaded[st], (j / kStages) & 1) &&
+                                       mbar_wait_cluster(&bar.v_free[rs], ((j / kRecv) & 1) ^ 1));
       if (!ok) break;
-      fence_proxy_async_smem();  // the producers' cp.async writes -> the bulk copy and the MMAs
-      if (lane == 0) mbar_arrive_expect_tx(&bar.kv_full[st], kFwdBytes);
-      ok = __all_sync(0xffffffffu, mbar_wait_cluster(&peer_free[st], ((j / kStages) & 1) ^ 1));
+      fence_proxy_async_smem();  // the producers' cp.async writes -> the bulk copy
+      if (lane == 0)
+        bulk_copy_to_peer(map_peer(smem_base + kOffRecv + rs * kHalfBytes, peer), smem + kOffStages + st * kStageBytes,
+                          kHalfBytes, map_peer(smem_u32(&bar.v_full[rs]), peer));
+      __syncwarp();
+    }
+    if (!ok) set_abort(bar, a.dev_error);
+  } else if (!score && warp == 8) {
+    // ------------------------------------------------- value CTA forwarder
+    // Own slot j % kOwn (chunks 4-7) -> the score CTA's stage of tile j, once
+    // that stage is free (tile j - 5 done there) and no longer holds Q.
+    bool ok = __all_sync(0xffffffffu, mbar_wait_cluster(&bar.q_gone, 0));
+    for (int j = 0; j < ntiles && ok; ++j) {
+      const int st = j % kStages, os = j % kOwn;
+      ok = __all_sync(0xffffffffu, mbar_wait(&bar.own_loaded[os], (j / kOwn) & 1) &&
+                                       mbar_wait_cluster(&bar.s_done[st], ((j / kStages) & 1) ^ 1));
       if (!ok) break;
-      if (lane == 0) {
-        const uint32_t src = smem_base + kOffStages + st * kStageBytes + off;
-        bulk_copy_to_peer(map_peer(src, peer), smem + kOffStages + st * kStageBytes + off, kFwdBytes,
-                          map_peer(smem_u32(&bar.kv_full[st]), peer));
-      }
+      fence_proxy_async_smem();  // the producers' cp.async writes -> the bulk copy
+      if (lane == 0)
+        bulk_copy_to_peer(map_peer(smem_base + kOffStages + st * kStageBytes + 4 * kChunkBytes, peer),
+                          smem + kOffOwn + os * kHalfBytes, kHalfBytes, map_peer(smem_u32(&bar.kv_full[st]), peer));
       __syncwarp();
     }
     if (!ok) set_abort(bar, a.dev_error);
   } else if (!score && warp == 9) {
-    // ---------------------------------------------------------------- acks
-    // Tell the score CTA when its chunks 0-3 of tile j have landed here, so
-    // that it may reuse the stage they were copied from.
+    // ------------------------------------------------- receive-ring arrivals
+    // When tile j's chunks 0-3 land, re-arm the slot for tile j + kRecv (that
+    // fill needs PV(j) first, so it cannot complete before this) and tell
+    // both CTAs that the score CTA's stage of tile j has been read.
     bool ok = true;
     for (int j = 0; j < ntiles && ok; ++j) {
-      const int st = j % kStages;
-      ok = __all_sync(0xffffffffu, mbar_wait_cluster(&bar.kv_full[st], (j / kStages) & 1));
-      if (ok && lane == 0) mbar_arrive_remote(map_peer(smem_u32(&bar.s_done[st]), peer));
+      const int st = j % kStages, vs = j % kRecv;
+      ok = __all_sync(0xffffffffu, mbar_wait_cluster(&bar.v_full[vs], (j / kRecv) & 1));
+      if (ok && lane == 0) {
+        mbar_arrive_expect_tx(&bar.v_full[vs], kHalfBytes);
+        mbar_arrive(&bar.s_done[st]);
+        mbar_arrive_remote(map_peer(smem_u32(&bar.s_done[st]), peer));
+      }
       __syncwarp();
     }
     if (!ok) set_abort(bar, a.dev_error);
@@ -357,12 +394,11 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(DecodeArgs a) {
       const int st = j % kStages, u = j / kSBuf;
       // s_free first: once the softmax has read S(j - 3) it has read every
       // earlier tile, so the stage's previous fill (tile j - 5) is consumed
-      // and the kv_full parity below can only mean tile j
+      // and the kv_loaded / kv_full parities below can only mean tile j
       ok = __all_sync(0xffffffffu, mbar_wait(&bar.s_free[b], (u & 1) ^ 1) &&
+                                       mbar_wait(&bar.kv_loaded[st], (j / kStages) & 1) &&
                                        mbar_wait_cluster(&bar.kv_full[st], (j / kStages) & 1));
       if (!ok) break;
-      // the value CTA's chunks 4-7 of tile j have landed: its stage may refill
-      if (half == 1 && lane == 0) mbar_arrive_remote(map_peer(smem_u32(&bar.v_done[st]), peer));
       // rows that were not loaded are zero and only reach S columns the
       // softmax masks; the stage's mask travels with the S slot, since the
       // stage itself is refilled as soon as both halves of S are done
@@ -472,19 +508,21 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(DecodeArgs a) {
   } else if (!score && warp == 10) {
     // -------------------------------------------------------- PV MMA issuer
     // O accumulates across tiles, so PV(j) is issued in order by one thread.
-    // P (K-major, 64-byte swizzle) and V (the stage's chunks 0-7 read
-    // MN-major: N atoms = 4 KB chunks, K = tokens in 8-row groups 1 KB
-    // apart) both come from shared memory.  Rows that were not loaded are
-    // zero, so P = 0 never meets a NaN/Inf value.
+    // P (K-major, 64-byte swizzle) and V (value dims 0-255 from the receive
+    // slot, 256-511 from the own slot, each read MN-major: N atoms = 4 KB
+    // chunks, K = tokens in 8-row groups 1 KB apart) both come from shared
+    // memory.  Rows that were not loaded are zero, so P = 0 never meets a
+    // NaN/Inf value.
     const uint32_t id_o = idesc_bf16(128, 256, 0, 1);
-    const uint64_t dv = smem_desc(smem_base + kOffStages, kChunkBytes, 1024, kSwizzle128B);
+    const uint64_t dv = smem_desc(smem_base, kChunkBytes, 1024, kSwizzle128B);
     const uint64_t dp = smem_desc(smem_base + kOffP, 16, 512, kSwizzle64B);
     bool ok = true;
     for (int j = 0; j < ntiles; ++j) {
-      const int st = j % kStages, slot = j % kPSlots;
+      const int vs = j % kRecv, os = j % kOwn, slot = j % kPSlots;
       ok = __all_sync(0xffffffffu, mbar_wait(&bar.p_ok[slot], (j / kPSlots) & 1) &&
                                        mbar_wait_cluster(&bar.p_full[slot], (j / kPSlots) & 1) &&
-                                       mbar_wait_cluster(&bar.kv_full[st], (j / kStages) & 1));
+                                       mbar_wait_cluster(&bar.v_full[vs], (j / kRecv) & 1) &&
+                                       mbar_wait(&bar.own_loaded[os], (j / kOwn) & 1));
       if (!ok) break;
       // the slot's next fill (tile j + kPSlots) cannot start before PV(j)
       // frees it, i.e. after this arm
@@ -492,15 +530,17 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(DecodeArgs a) {
       fence_proxy_async_smem();
       tc_fence_after();
       if (lane == 0) {
-        const uint64_t so = static_cast<uint64_t>((st * kStageBytes) >> 4);
+        const uint64_t sv[2] = {static_cast<uint64_t>((kOffRecv + vs * kHalfBytes) >> 4),
+                                static_cast<uint64_t>((kOffOwn + os * kHalfBytes) >> 4)};
         const uint64_t po = static_cast<uint64_t>((slot * kPSlotBytes) >> 4);
 #pragma unroll
         for (int k = 0; k < 2; ++k)
 #pragma unroll
           for (int n = 0; n < 2; ++n)
-            mma_ss(tbase + kColO + 256 * n, dp + po + ((32 * k) >> 4),
-                   dv + so + ((4 * n * kChunkBytes + 2048 * k) >> 4), id_o, (j > 0 || k > 0) ? 1u : 0u);
-        mma_commit_mc(&bar.v_done[st], 0x3);
+            mma_ss(tbase + kColO + 256 * n, dp + po + ((32 * k) >> 4), dv + sv[n] + ((2048 * k) >> 4), id_o,
+                   (j > 0 || k > 0) ? 1u : 0u);
+        mma_commit_mc(&bar.v_free[vs], 0x3);
+        mma_commit(&bar.own_free[os]);
         mma_commit_mc(&bar.p_free[slot], 0x3);
         mma_commit(&bar.pv_done[slot]);
         if (j == ntiles - 1) mma_commit(&bar.o_final);
@@ -552,7 +592,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(DecodeArgs a) {
       }
     }
     // ------------------------------------------------------------ epilogue
-    // warps 0-3 write value dims [0, 256), warps 4-7 dims [256, 512)
+    // warps 0-3 write value dims [0, 256), warps 4-7 dims [256, 512).  Each
+    // 32-column block of a warp's 32 rows goes through a padded shared-memory
+    // transpose (stage 0 is idle by now), so that every store instruction
+    // writes 128 contiguous bytes of one O row.
     if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&bar.o_final, 0) && mbar_wait_cluster(&bar.fin_l, 0));
     if (ok) ok = !__any_sync(0xffffffffu, aborted(bar));
     if (!ok) {
@@ -561,23 +604,38 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(DecodeArgs a) {
       tc_fence_after();
       const float inv = *reinterpret_cast<const volatile float*>(smem + kOffFin + 4 * h);
       const int c0 = (warp >> 2) * 8;
-      float* orow = a.O_dst + (pair0 + h) * kLatent;
+      // 32 rows x 32 fp32 per block, rows 144 B apart (16-byte aligned; a
+      // warp's 16-byte writes and reads then hit 4 banks groups at most)
+      float* scr = reinterpret_cast<float*>(smem + kOffStages) + warp * (32 * 36);
+      float* orow0 = a.O_dst + (pair0 + q4 * 32) * kLatent;
+      const int nrows = min(32, a.H - q4 * 32);
       for (int c = c0; c < c0 + 8; ++c) {
         uint32_t o[32];
         tmem_ld32(lane_addr + kColO + 32 * c, o);
         tmem_wait_ld();
-        if (h < a.H) {
 #pragma unroll
-          for (int i = 0; i < 8; ++i)
-            reinterpret_cast<float4*>(orow + 32 * c)[i] =
-                make_float4(__uint_as_float(o[4 * i]) * inv, __uint_as_float(o[4 * i + 1]) * inv,
-                            __uint_as_float(o[4 * i + 2]) * inv, __uint_as_float(o[4 * i + 3]) * inv);
+        for (int k = 0; k < 8; ++k)
+          *reinterpret_cast<float4*>(scr + lane * 36 + 4 * k) =
+              make_float4(__uint_as_float(o[4 * k]) * inv, __uint_as_float(o[4 * k + 1]) * inv,
+                          __uint_as_float(o[4 * k + 2]) * inv, __uint_as_float(o[4 * k + 3]) * inv);
+        __syncwarp();
+        // lane l: row 4 m + l / 8, columns 4 (l % 8) .. + 3 of the block
+#pragma unroll
+        for (int m = 0; m < 8; ++m) {
+          const int rr = 4 * m + (lane >> 3);
+          if (rr < nrows)
+            *reinterpret_cast<float4*>(orow0 + rr * kLatent + 32 * c + 4 * (lane & 7)) =
+                *reinterpret_cast<const float4*>(scr + rr * 36 + 4 * (lane & 7));
         }
+        __syncwarp();
       }
     }
   }
 
   // ------------------------------------------------------------- teardown
+  // the grid that consumes O_part / lse_part may start launching now; it
+  // waits for this grid's completion before reading them
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const bool failed = aborted(bar);
   tc_fence_before();
   __syncthreads();
