@@ -36,6 +36,28 @@ METRIC = "MLA DCP decode KV tokens/s + combine GB/s, % of GB300 HBM roofline"
 UNIT = "KV tokens/s"
 L2_FLUSH_BYTES = 512 << 20
 KV_ROW_BYTES = 576 * 2
+# DRAM bytes (read + write) of one tensor-core decode launch on the 120k
+# long-context workload, from one ncu capture of that launch.  They describe
+# only the kernel source they were taken on, so they are reported only while
+# that file's hash matches.
+MEASURED_TRAFFIC = {
+    "workload": "long_ctx_120k_b1_d8_i1",
+    "source": "mla_decode_context_gb300/csrc/dcp_decode_tc.cu",
+    "sha256": "3e93861f87354e6182ccc99da385ab426f62ac728afdb7e9de0f4a4f2bd75180",
+    "bytes": 138488064 + 3658752,
+}
+
+
+def measured_traffic(workload: str):
+    import hashlib
+    if workload != MEASURED_TRAFFIC["workload"] or os.environ.get("DCP_FORCE_SIMT") == "1":
+        return None
+    try:
+        with open(os.path.join(ROOT, MEASURED_TRAFFIC["source"]), "rb") as f:
+            digest = hashlib.sha256(f.read()).hexdigest()
+    except OSError:
+        return None
+    return MEASURED_TRAFFIC["bytes"] if digest == MEASURED_TRAFFIC["sha256"] else None
 
 
 def peaks():
@@ -323,7 +345,7 @@ def run_gb300(args, spec):
             "roofline": {"bound": "hbm", "kernel": "dcp_mla_decode_partial", "achieved": achieved,
                          "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                          "peak_source": peak_kind + " (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
-                         else "fallback 6.8 TB/s", "traffic": None,
+                         else "fallback 6.8 TB/s", "traffic": measured_traffic(spec.name),
                          "algorithmic_bytes_per_launch": dbytes},
             "e2e": {"value": ws * tokens / (e2e_avg * 1e-3), "unit": UNIT, "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "note": "host-pinned per-step inputs (q, block table, "
