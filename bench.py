@@ -179,6 +179,12 @@ def max_over_ranks(x: float, device) -> float:
     return float(t.item())
 
 
+def aggregate_rate(world_size: int, tokens_per_rank: int, max_ms: float) -> float:
+    """Whole-job rate of a weak-scaling replica run: every rank processes the
+    same workload, and the job takes as long as its slowest rank."""
+    return world_size * tokens_per_rank / (max_ms * 1e-3)
+
+
 def barrier():
     import torch.distributed as dist
     if dist.is_available() and dist.is_initialized():
@@ -331,7 +337,7 @@ def run_gb300(args, spec):
     if rank == 0:
         rate, passes, secs = cpu_oracle_rate(inp)
         res = {
-            "metric": METRIC, "value": ws * tokens / (step_ms * 1e-3), "unit": UNIT, "n_gpus": ws,
+            "metric": METRIC, "value": aggregate_rate(ws, tokens, step_ms), "unit": UNIT, "n_gpus": ws,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_ms,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": dcp.compute_dtype(), "data": "synthetic",
@@ -347,7 +353,7 @@ def run_gb300(args, spec):
                          "peak_source": peak_kind + " (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
                          else "fallback 6.8 TB/s", "traffic": measured_traffic(spec.name),
                          "algorithmic_bytes_per_launch": dbytes},
-            "e2e": {"value": ws * tokens / (e2e_avg * 1e-3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+            "e2e": {"value": aggregate_rate(ws, tokens, e2e_avg), "unit": UNIT, "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "note": "host-pinned per-step inputs (q, block table, "
                     "seq_lens, query_start_loc) copied in and out/out_lse copied back inside the timed "
                     "region; the paged KV cache is resident device state"},
