@@ -66,8 +66,8 @@ constexpr int kStages = 5;                       // score CTA: stage ring
 constexpr int kNch = 9;                          // 64-dim chunks of a latent row
 constexpr int kChunkBytes = kTile * 128;         // 32 rows x 64 bf16, 128B-swizzled
 constexpr int kStageBytes = kNch * kChunkBytes;  // 36 KB
-constexpr int kProdWarp0 = 11, kProdWarps = 8;   // producer warps
-constexpr int kProdThreads = 32 * kProdWarps;
+constexpr int kProdWarp0 = 11, kProdWarps = 8;   // producer warps: two groups of 4 (alternate tiles)
+constexpr int kGroupThreads = 32 * kProdWarps / 2;
 constexpr int kHalfBytes = 4 * kChunkBytes;      // 4 chunks: forwarded each way per tile
 constexpr int kOwn = 8;                          // value CTA: own ring slots (chunks 4-7)
 constexpr int kRecv = 3;                         // value CTA: receive ring slots (chunks 0-3)
@@ -87,12 +87,12 @@ constexpr uint32_t kColO = 0;    // value: 512 columns of O
 constexpr uint32_t kTmemCols = 512;
 
 struct __align__(8) Bars {
-  uint64_t kv_loaded[kStages];  // score: own rows of tile j landed (every producer thread)
+  uint64_t kv_loaded[kStages];  // score: own rows of tile j landed (every thread of tile j's producer group)
   uint64_t kv_full[kStages];    // score: the value CTA's 16 KB of tile j landed (armed by a producer)
   // s_done (both CTAs): the score CTA's stage of tile j is free again: both
   // halves of S(j) done and tile j's V part has landed in the value CTA
   uint64_t s_done[kStages];
-  uint64_t own_loaded[kOwn];    // value: rows of tile j in own slot j % kOwn (every producer thread)
+  uint64_t own_loaded[kOwn];    // value: rows of tile j in own slot j % kOwn (every thread of its producer group)
   uint64_t own_free[kOwn];      // value: PV(j) done with own slot j % kOwn
   uint64_t v_full[kRecv];       // value: chunks 0-3 of tile j landed in receive slot j % kRecv
   uint64_t v_free[kRecv];       // score (multicast commit of PV(j)): receive slot j % kRecv may refill
@@ -179,11 +179,11 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(DecodeArgs a) {
   // ---------------------------------------------------------------- setup
   if (threadIdx.x == 0) {
     for (int i = 0; i < kStages; ++i) {
-      mbar_init(&bar.kv_loaded[i], kProdThreads);
+      mbar_init(&bar.kv_loaded[i], kGroupThreads);
       mbar_init(&bar.kv_full[i], 1);
       mbar_init(&bar.s_done[i], 3);
     }
-    for (int i = 0; i < kOwn; ++i) { mbar_init(&bar.own_loaded[i], kProdThreads); mbar_init(&bar.own_free[i], 1); }
+    for (int i = 0; i < kOwn; ++i) { mbar_init(&bar.own_loaded[i], kGroupThreads); mbar_init(&bar.own_free[i], 1); }
     for (int i = 0; i < kRecv; ++i) { mbar_init(&bar.v_full[i], 1); mbar_init(&bar.v_free[i], 1); }
     for (int i = 0; i < kSBuf; ++i) { mbar_init(&bar.s_full[i], 3); mbar_init(&bar.s_free[i], 4); }
     mbar_init(&bar.q_staged, 256);
@@ -262,48 +262,52 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(DecodeArgs a) {
 
   if (warp >= kProdWarp0) {
     // ----------------------------------------------------------- producers
-    // The 256 threads copy the 16-byte units of the CTA's own chunks of the
-    // tile's rows (upr units per row: chunks 0-3 + 8 = 40 into the score
-    // CTA's stage, chunks 4-7 = 32 into the value CTA's own slot, laid out
-    // as the stage's chunks 4-7 are); unit p = i * 256 + t, so
+    // Two groups of four warps take alternate tiles (a producer thread's
+    // issue is latency-bound, so two tiles are in flight at once).  The 128
+    // threads of a group copy the 16-byte units of the CTA's own chunks of
+    // the tile's rows (upr units per row: chunks 0-3 + 8 = 40 into the
+    // score CTA's stage, chunks 4-7 = 32 into the value CTA's own slot, laid
+    // out as the stage's chunks 4-7 are); unit p = i * 128 + t, so
     // consecutive lanes read consecutive bytes of a row.  Lane i of each
-    // warp resolves row i of the tile (shard token -> cache row).  Each
-    // thread's copies of a tile arrive on kv_loaded by themselves when they
-    // complete; the consumers fence them into the async proxy.
-    const int t = threadIdx.x - 32 * kProdWarp0;
+    // warp resolves row i of the tile (shard token -> cache row), one of
+    // the group's tiles ahead.  Each thread's copies of a tile arrive on
+    // kv_loaded / own_loaded by themselves when they complete; the
+    // consumers fence them into the async proxy.
+    const int group = (warp - kProdWarp0) >> 2;
+    const bool leader = ((warp - kProdWarp0) & 3) == 0;  // first warp of the group
+    const int t = (warp - kProdWarp0 - 4 * group) * 32 + lane;
     const int upr = score ? 40 : 32;
-    const int per_thread = kTile * upr / kProdThreads;
+    const int per_thread = kTile * upr / kGroupThreads;
     const unsigned char* kvb = reinterpret_cast<const unsigned char*>(a.kv);
     uint64_t* own_free = score ? bar.s_done : bar.own_free;
     uint64_t* own_loaded = score ? bar.kv_loaded : bar.own_loaded;
     const int nslots = score ? kStages : kOwn;
-    // lane i resolves row i of a tile one tile ahead (the block-table load
-    // is consumed an iteration later, so its latency stays off the copies)
+    const int32_t DI = a.D * a.I, dI = d * a.I;
     bool in_n = false;
     int32_t pos_n = 0, blk_n = -1;
-    auto fetch = [&](int jj) {
+    auto fetch = [&](int jj) {  // positions fit in 32 bits (seq_lens are int32)
       const int32_t l = lo + jj * kTile + lane;
       in_n = l < hi;
-      pos_n = in_n ? static_cast<int32_t>(local_to_global(l, d, a.D, a.I)) : 0;
+      pos_n = in_n ? (l / a.I) * DI + dI + l % a.I : 0;
       blk_n = in_n ? __ldg(trow + pos_n / a.block_size) : -1;
     };
-    fetch(0);
+    fetch(group);
     bool ok = true;
     if (score) ok = __all_sync(0xffffffffu, mbar_wait(&bar.q_ready, 0));
-    for (int j = 0; j < ntiles && ok; ++j) {
+    for (int j = group; j < ntiles && ok; j += 2) {
       const bool in = in_n;
       const int32_t pos = pos_n, blk = blk_n;
-      if (j + 1 < ntiles) fetch(j + 1);
+      if (j + 2 < ntiles) fetch(j + 2);
       const int st = j % nslots;
       ok = __all_sync(0xffffffffu, mbar_wait(&own_free[st], ((j / nslots) & 1) ^ 1));
       if (ok) ok = !__any_sync(0xffffffffu, aborted(bar));
       if (!ok) break;
       const bool valid = in && blk >= 0 && blk < a.num_blocks;
-      if (in && !valid && score && warp == kProdWarp0) report(a.dev_error, DCP_DEVERR_BAD_BLOCK);
+      if (in && !valid && score && leader) report(a.dev_error, DCP_DEVERR_BAD_BLOCK);
       const int64_t roff =
           valid ? (static_cast<int64_t>(blk) * a.block_size + pos % a.block_size) * (kKDim * 2) : 0;
       const uint32_t mask = __ballot_sync(0xffffffffu, valid);
-      if (score && warp == kProdWarp0 && lane == 0) {
+      if (score && leader && lane == 0) {
         bar.mask[st] = mask;
         // tile j - 5 is done with the stage, so kv_full's previous phase is
         // complete: arm it for the value CTA's 16 KB of tile j
@@ -312,9 +316,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(DecodeArgs a) {
       // the value CTA's own slot holds chunks 4-7 at chunk offsets 0-3
       const uint32_t sbase = score ? smem_base + kOffStages + st * kStageBytes
                                    : smem_base + kOffOwn + st * kHalfBytes - 4 * kChunkBytes;
-#pragma unroll 5
+#pragma unroll 10
       for (int i = 0; i < per_thread; ++i) {
-        const int p = i * kProdThreads + t;
+        const int p = i * kGroupThreads + t;
         const int row = score ? p / 40 : p >> 5;
         const int u = p - row * upr;
         const int c = score ? (u < 32 ? (u >> 3) : 8) : 4 + (u >> 3);  // chunk
