@@ -36,8 +36,9 @@
 // 8-row boxes, which capped the stream well below HBM bandwidth; a single
 // SM's cp.async stream tops out near 16 B/clk, hence the split.)
 //
-// Warp roles (608 threads):
-//   warps 0-3   score: Q load, then softmax (thread = head = TMEM lane)
+// Warp roles (736 threads):
+//   warps 0-3   score: Q load, then softmax group 0 (thread = head = TMEM
+//                      lane; even tiles)
 //               value: max tracking and O rescale; epilogue columns 0-255
 //   warps 4-9   score: (4-7 also Q load) S issuers: warp 4 + 2i + k issues
 //                      half k of S for tiles j = i mod 3 into S slot i (a
@@ -49,6 +50,7 @@
 //                      ring); value: PV issuer
 //   warps 11-18 both:  producers (cp.async; the score CTA's wait until Q has
 //                      left stages 0-3 for TMEM)
+//   warps 19-22 score: softmax group 1 (odd tiles)
 // Every wait is bounded (a timeout sets DCP_DEVERR_TIMEOUT and ends the unit).
 #include "dcp_kernels.h"
 #include "dcp_sm100.cuh"
@@ -69,15 +71,16 @@ constexpr int kStageBytes = kNch * kChunkBytes;  // 36 KB
 constexpr int kProdWarp0 = 11, kProdWarps = 8;   // producer warps: two groups of 4 (alternate tiles)
 constexpr int kGroupThreads = 32 * kProdWarps / 2;
 constexpr int kHalfBytes = 4 * kChunkBytes;      // 4 chunks: forwarded each way per tile
-constexpr int kOwn = 8;                          // value CTA: own ring slots (chunks 4-7)
-constexpr int kRecv = 3;                         // value CTA: receive ring slots (chunks 0-3)
+constexpr int kOwn = 7;                          // value CTA: own ring slots (chunks 4-7)
+constexpr int kRecv = 4;                         // value CTA: receive ring slots (chunks 0-3)
 constexpr int kSBuf = 3;                         // S slots (two 32-column halves each) in TMEM
 constexpr int kPSlots = 4;                       // P slots in the value CTA
 constexpr int kPBytes = 128 * kTile * 2;         // P tile: 128 rows x 32 bf16, 64B-swizzled
 constexpr int kPWarpBytes = kPBytes / 4;         // one softmax warp's 32 rows
 constexpr int kPSlotBytes = 9216;                // P tile + running max per head (+ pad)
 constexpr uint32_t kPTx = kPBytes + 128 * 4;     // bytes that fill one P slot
-constexpr int kThreads = 32 * (kProdWarp0 + kProdWarps);
+constexpr int kSmWarp1 = kProdWarp0 + kProdWarps;  // score: second softmax group (4 warps)
+constexpr int kThreads = 32 * (kSmWarp1 + 4);
 constexpr float kRescaleLog2 = 8.0f;
 
 // TMEM columns
@@ -108,6 +111,8 @@ struct __align__(8) Bars {
   uint64_t o_final;           // value: last PV complete
   uint64_t fin_l;             // value: 1/l of every head arrived from the score CTA
   uint64_t fin[1 + 2 * kSBuf];  // each issuing warp's MMAs complete
+  uint64_t m_pub[2];          // score: running max after tile j published (phase j / 2 of m_pub[j & 1]; 4 warps)
+  uint64_t sm_fin;            // score: both softmax groups' final l and m written (8 warps)
   uint32_t mask[kStages];     // valid rows of the tile in each stage
   uint32_t smask[kSBuf];      // score: valid rows of the tile in each S slot
   uint32_t tmem;
@@ -119,7 +124,8 @@ constexpr int kOffOwn = 0;                               // value: own ring
 constexpr int kOffRecv = kOwn * kHalfBytes;              // value: receive ring
 constexpr int kOffP = kStages * kStageBytes;             // value: P slots; score: P staging
 constexpr int kOffFin = kOffP + kPSlots * kPSlotBytes;   // value: 1/l per head
-constexpr int kOffBars = kOffFin + 512;
+constexpr int kOffSm = kOffFin + 512;                    // score: softmax group hand-off
+constexpr int kOffBars = kOffSm + 5 * 128 * 4;
 constexpr int kSmemBytes = kOffBars + static_cast<int>(sizeof(Bars)) + 1024;  // + alignment slack
 static_assert(kSmemBytes <= 232448, "exceeds the 227 KB of shared memory per CTA");
 static_assert(kPSlotBytes % 1024 == 0 && kOffP % 1024 == 0, "P tiles must sit on swizzle-atom boundaries");
@@ -198,6 +204,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(DecodeArgs a) {
     mbar_init(&bar.o_final, 1);
     mbar_init(&bar.fin_l, 1);
     for (int i = 0; i < 1 + 2 * kSBuf; ++i) mbar_init(&bar.fin[i], 1);
+    mbar_init(&bar.m_pub[0], 4);
+    mbar_init(&bar.m_pub[1], 4);
+    mbar_init(&bar.sm_fin, 8);
     bar.abort = 0;
     fence_mbar_init();
     if (!score) {
@@ -260,7 +269,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(DecodeArgs a) {
   const uint32_t smem_base = smem_u32(smem);
   int pdone = 0;  // value, warps 0-3: P tiles received
 
-  if (warp >= kProdWarp0) {
+  if (warp >= kProdWarp0 && warp < kSmWarp1) {
     // ----------------------------------------------------------- producers
     // Two groups of four warps take alternate tiles (a producer thread's
     // issue is latency-bound, so two tiles are in flight at once).  The 128
@@ -428,16 +437,24 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(DecodeArgs a) {
     if (lane == 0) mma_commit(&bar.fin[1 + 2 * b + half]);
     __syncwarp();
     mbar_wait(&bar.fin[1 + 2 * b + half], 0);
-  } else if (score && warp < 4) {
+  } else if (score && (warp < 4 || warp >= kSmWarp1)) {
     // ------------------------------------------------------------- softmax
-    const int h = threadIdx.x;
-    const uint32_t lane_addr = tbase + (static_cast<uint32_t>(warp * 32) << 16);
+    // Two groups of four warps take alternate tiles.  The running max per
+    // head passes from tile to tile through shared memory (m_sh, published
+    // on m_pub); each group keeps the normaliser of its own tiles and
+    // rescales it whenever it learns of a new max.  The two normalisers are
+    // added at the end.
+    const int sg = warp < 4 ? 0 : 1, q4 = warp & 3;
+    const int h = q4 * 32 + lane;
+    const uint32_t lane_addr = tbase + (static_cast<uint32_t>(q4 * 32) << 16);
+    float* m_sh = reinterpret_cast<float*>(smem + kOffSm);  // [128]: running max after the latest tile
+    float* fin_sh = m_sh + 128;                             // [group][l, m][128]
     const float sl2 = a.scale * kLog2e;
     float m_used = -INFINITY, l_sum = 0.f;
     const int sw = (h >> 1) & 3;  // 64-byte swizzle of row h
     const uint32_t p_row = static_cast<uint32_t>((h >> 3) * 512 + (h & 7) * 64);
     bool ok = true;
-    for (int j = 0; j < ntiles; ++j) {
+    for (int j = sg; j < ntiles; j += 2) {
       const int b = j % kSBuf, slot = j % kPSlots;
       ok = __all_sync(0xffffffffu, mbar_wait(&bar.s_full[b], (j / kSBuf) & 1));
       if (!ok) break;
@@ -464,6 +481,16 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(DecodeArgs a) {
       for (int i = 0; i < 8; ++i) mx[i] = fmaxf(fmaxf(sc[4 * i], sc[4 * i + 1]), fmaxf(sc[4 * i + 2], sc[4 * i + 3]));
       const float tmax = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
                                fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))) * sl2;
+      if (j > 0) {
+        // the running max after tile j - 1 (the other group's); it only grows
+        ok = __all_sync(0xffffffffu, mbar_wait(&bar.m_pub[(j - 1) & 1], ((j - 1) >> 1) & 1));
+        if (!ok) break;
+        const float m_prev = *reinterpret_cast<volatile float*>(&m_sh[h]);
+        if (m_prev != m_used) {
+          if (m_used != -INFINITY) l_sum *= ex2_approx(m_used - m_prev);
+          m_used = m_prev;
+        }
+      }
       // lazy rescale: the running max only moves when it would grow by more
       // than 2^8 (the value CTA rescales O by the same factor)
       const bool grow = m_used == -INFINITY ? (tmax != -INFINITY) : (tmax > m_used + kRescaleLog2);
@@ -471,6 +498,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(DecodeArgs a) {
         if (m_used != -INFINITY) l_sum *= ex2_approx(m_used - tmax);
         m_used = tmax;
       }
+      m_sh[h] = m_used;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bar.m_pub[j & 1]);
       // p = 2^(s * scale * log2e - m); masked (-inf) scores give exactly 0,
       // and nothing is live while m is still -inf
       const float nm = m_used == -INFINITY ? 0.f : -m_used;
@@ -498,16 +528,32 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(DecodeArgs a) {
       const uint32_t peer_slot = map_peer(smem_base + kOffP + slot * kPSlotBytes, peer);
       const uint32_t peer_full = map_peer(smem_u32(&bar.p_full[slot]), peer);
       if (lane == 0)
-        bulk_copy_to_peer(peer_slot + warp * kPWarpBytes, stg + warp * kPWarpBytes, kPWarpBytes, peer_full);
+        bulk_copy_to_peer(peer_slot + q4 * kPWarpBytes, stg + q4 * kPWarpBytes, kPWarpBytes, peer_full);
       st_async_peer_b32(peer_slot + kPBytes + 4 * h, __float_as_uint(m_used), peer_full);
     }
+    // both groups' normalisers meet here; group 0 finishes the unit
+    fin_sh[(2 * sg) * 128 + h] = l_sum;
+    fin_sh[(2 * sg + 1) * 128 + h] = m_used;
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&bar.sm_fin);
     if (!ok) {
       set_abort(bar, a.dev_error);
-    } else {
-      const bool live = l_sum > 0.f;
-      st_async_peer_b32(map_peer(smem_base + kOffFin + 4 * h, peer), __float_as_uint(live ? 1.f / l_sum : 0.f),
-                        map_peer(smem_u32(&bar.fin_l), peer));
-      if (h < a.H) a.lse_dst[pair0 + h] = live ? (m_used + log2f(l_sum)) * kLn2 : -INFINITY;
+    } else if (sg == 0) {
+      ok = __all_sync(0xffffffffu, mbar_wait(&bar.sm_fin, 0)) && !__any_sync(0xffffffffu, aborted(bar));
+      if (!ok) {
+        set_abort(bar, a.dev_error);
+      } else {
+        const float l1 = *reinterpret_cast<volatile float*>(&fin_sh[2 * 128 + h]);
+        const float m1 = *reinterpret_cast<volatile float*>(&fin_sh[3 * 128 + h]);
+        const float mf = fmaxf(m_used, m1);  // the running max after the last tile
+        float l = 0.f;
+        if (m_used != -INFINITY) l += l_sum * ex2_approx(m_used - mf);
+        if (m1 != -INFINITY) l += l1 * ex2_approx(m1 - mf);
+        const bool live = l > 0.f;
+        st_async_peer_b32(map_peer(smem_base + kOffFin + 4 * h, peer), __float_as_uint(live ? 1.f / l : 0.f),
+                          map_peer(smem_u32(&bar.fin_l), peer));
+        if (h < a.H) a.lse_dst[pair0 + h] = live ? (mf + log2f(l)) * kLn2 : -INFINITY;
+      }
     }
   } else if (!score && warp == 10) {
     // -------------------------------------------------------- PV MMA issuer
