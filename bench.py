@@ -273,7 +273,7 @@ def run_gb300(args, spec):
         combine()
     torch.cuda.synchronize()
     check_device_flags("warm-up")
-    launches_per_step = 2 + (1 if wsz else 0)
+    launches_per_step = 1 + dcp.dcp_decode_kernel_launches(B, T, H, D, I, msl, mql, work.numel() if work is not None else 0)
 
     # ---- device-timed steps (inputs resident, L2 flushed before each) ----
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]

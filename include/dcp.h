@@ -100,12 +100,28 @@ int32_t dcp_shard_of(int64_t pos, int32_t D, int32_t interleave);
 int32_t dcp_local_len(int32_t L, int32_t d, int32_t D, int32_t interleave);
 
 /*
- * Bytes of device workspace dcp_mla_decode_partial needs for these sizes on
- * the CURRENT device (the split-KV plan depends on its SM count).  Zero means
- * `workspace` may be NULL.  Returns (size_t)-1 on invalid arguments.
+ * Bytes of device workspace dcp_mla_decode_partial should get for these sizes
+ * on the CURRENT device (the split-KV plan depends on its SM count): the
+ * split partials plus one int32 per work unit for the order in which the
+ * units start (long ones first when they do not all fit on the GPU at once).
+ * A workspace that covers only the split partials is accepted (units then
+ * start in index order); with no split partials it may be NULL.  Returns
+ * (size_t)-1 on invalid arguments.
  */
 size_t dcp_decode_workspace_size(int32_t B, int32_t T, int32_t H, int32_t D,
                                  int32_t max_seq_len, int32_t max_q_len);
+
+/*
+ * Number of kernels one dcp_mla_decode_partial call with these sizes and this
+ * workspace size launches on the CURRENT device: the decode, plus the merge of
+ * the split partials when the long-context split is used, plus the ordering
+ * of the work units when there are more of them than fit on the GPU at once
+ * (and the workspace has room for it).  0 when B or T is 0; -1 on invalid
+ * arguments.  For callers that count or capture launches; no page has a
+ * counterpart.
+ */
+int32_t dcp_decode_kernel_launches(int32_t B, int32_t T, int32_t H, int32_t D, int32_t interleave,
+                                   int32_t max_seq_len, int32_t max_q_len, size_t workspace_bytes);
 
 /*
  * Absorbed-MLA decode attention split over D context shards.

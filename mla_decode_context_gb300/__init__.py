@@ -50,6 +50,7 @@ EXPORTS = [
     ("dcp_shard_of", _I32, [_I64, _I32, _I32]),
     ("dcp_local_len", _I32, [_I32, _I32, _I32, _I32]),
     ("dcp_decode_workspace_size", _SZ, [_I32, _I32, _I32, _I32, _I32, _I32]),
+    ("dcp_decode_kernel_launches", _I32, [_I32, _I32, _I32, _I32, _I32, _I32, _I32, _SZ]),
     ("dcp_mla_decode_partial", ctypes.c_int,
      [_P, _I64, _P, _I32, _I32, _P, _I32, _I64, _P, _P, _I32, _I32, _I32, _I32, _I32, _I32, _I32, _F,
       _P, _P, _P, _SZ, _P, _P]),
@@ -137,6 +138,14 @@ def dcp_decode_workspace_size(B: int, T: int, H: int, D: int, max_seq_len: int, 
     n = lib().dcp_decode_workspace_size(B, T, H, D, max_seq_len, max_q_len)
     if n == ctypes.c_size_t(-1).value:
         raise DCPError(1, "dcp_decode_workspace_size")
+    return n
+
+
+def dcp_decode_kernel_launches(B: int, T: int, H: int, D: int, interleave: int, max_seq_len: int,
+                               max_q_len: int, workspace_bytes: int) -> int:
+    n = lib().dcp_decode_kernel_launches(B, T, H, D, interleave, max_seq_len, max_q_len, workspace_bytes)
+    if n < 0:
+        raise DCPError(1, "dcp_decode_kernel_launches")
     return n
 
 

@@ -58,6 +58,12 @@ SplitPlan plan_splits(int32_t T, int32_t D, int32_t I, int32_t max_seq_len, int 
   return p;
 }
 
+// Tail of the workspace for the units' launch order (one int32 per unit).
+size_t order_workspace_bytes(const SplitPlan& p, int32_t T, int32_t D) {
+  const size_t units = static_cast<size_t>(p.splits < 1 ? 1 : p.splits) * D * T;
+  return (units * sizeof(int32_t) + 255) / 256 * 256;
+}
+
 size_t split_workspace_bytes(const SplitPlan& p, int32_t T, int32_t H, int32_t D) {
   if (p.splits <= 1) return 0;
   const size_t pairs = static_cast<size_t>(p.splits) * D * T * H;
@@ -70,6 +76,38 @@ size_t split_workspace_bytes(const SplitPlan& p, int32_t T, int32_t H, int32_t D
 }  // namespace dcp
 
 static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+namespace {
+// What one dcp_mla_decode_partial call with these sizes does on the current
+// device: its split plan, the workspace the split partials need, and which
+// kernels it launches.
+struct DecodeLaunch {
+  dcp::SplitPlan plan;
+  size_t need;       // split partials (required when plan.splits > 1)
+  size_t obytes;     // launch order of the units (optional tail)
+  bool simt;         // CUDA-core kernel instead of the tensor-core one
+  bool use_order;    // units start longest first (order kernel launched)
+};
+
+DecodeLaunch decode_launch(int32_t T, int32_t H, int32_t D, int32_t interleave, int32_t max_seq_len,
+                           bool have_workspace, size_t workspace_bytes) {
+  DecodeLaunch L{};
+  const int sms = dcp::current_sm_count();
+  L.plan = dcp::plan_splits(T, D, interleave, max_seq_len, sms);
+  L.need = dcp::split_workspace_bytes(L.plan, T, H, D);
+  L.obytes = dcp::order_workspace_bytes(L.plan, T, D);
+  dcp::DecodeArgs a{};
+  a.H = H;
+  a.plan = L.plan;
+  const char* force = std::getenv("DCP_FORCE_SIMT");  // 1: the CUDA-core reference kernel (A/B checks)
+  L.simt = (force && force[0] == '1') || !dcp::decode_tc_supported(a);
+  const int64_t units = static_cast<int64_t>(T) * D * L.plan.splits;
+  const int resident = dcp::decode_tc_resident_ctas();  // 0: no device to size against
+  L.use_order = !L.simt && resident > 0 && units > resident / 2 && have_workspace &&
+                workspace_bytes >= L.need + L.obytes;
+  return L;
+}
+}  // namespace
 
 extern "C" {
 
@@ -108,7 +146,7 @@ size_t dcp_decode_workspace_size(int32_t B, int32_t T, int32_t H, int32_t D, int
   // max_seq_len tokens, and the split count never exceeds split_cap(lmax).
   const int sms = dcp::current_sm_count();
   dcp::SplitPlan p{static_cast<int32_t>(dcp::split_cap(T, D, max_seq_len, sms)), 0};
-  return dcp::split_workspace_bytes(p, T, H, D);
+  return dcp::split_workspace_bytes(p, T, H, D) + dcp::order_workspace_bytes(p, T, D);
 }
 
 dcp_status_t dcp_mla_decode_partial(const void* q, int64_t q_stride_tok, const void* kv_cache,
@@ -132,9 +170,10 @@ dcp_status_t dcp_mla_decode_partial(const void* q, int64_t q_stride_tok, const v
   if ((static_cast<int64_t>(max_seq_len) + block_size - 1) / block_size > bt_width)
     return DCP_ERR_TABLE_TOO_NARROW;
 
-  const int sms = dcp::current_sm_count();
-  const dcp::SplitPlan plan = dcp::plan_splits(T, D, interleave, max_seq_len, sms);
-  const size_t need = dcp::split_workspace_bytes(plan, T, H, D);
+  const DecodeLaunch launch =
+      decode_launch(T, H, D, interleave, max_seq_len, workspace != nullptr, workspace_bytes);
+  const dcp::SplitPlan plan = launch.plan;
+  const size_t need = launch.need;
   if (need > 0 && (workspace_bytes < need || !workspace)) return DCP_ERR_WORKSPACE_TOO_SMALL;
   if (need > 0 && !aligned16(workspace)) return DCP_ERR_MISALIGNED;
 
@@ -169,10 +208,20 @@ dcp_status_t dcp_mla_decode_partial(const void* q, int64_t q_stride_tok, const v
     a.O_dst = O_part;
     a.lse_dst = lse_part;
   }
-  // DCP_FORCE_SIMT=1 selects the CUDA-core reference kernel (A/B checks)
-  const char* force = std::getenv("DCP_FORCE_SIMT");
-  const bool simt = (force && force[0] == '1') || !dcp::decode_tc_supported(a);
-  cudaError_t e = simt ? dcp::launch_decode_simt(a, st) : dcp::launch_decode_tc(a, st);
+  const bool simt = launch.simt;
+  a.unit_order = nullptr;
+  cudaError_t e = cudaSuccess;
+  if (launch.use_order) {
+    // more units than clusters that fit at once: start the long ones first
+    // (the order lives in the workspace past the split partials; a workspace
+    // without room for it keeps index order)
+    const int64_t units = static_cast<int64_t>(T) * D * plan.splits;
+    int32_t* order = reinterpret_cast<int32_t*>(static_cast<char*>(workspace) + need);
+    e = dcp::launch_unit_order(a, static_cast<int32_t>(units), order, st);
+    if (e != cudaSuccess) return DCP_ERR_CUDA;
+    a.unit_order = order;
+  }
+  e = simt ? dcp::launch_decode_simt(a, st) : dcp::launch_decode_tc(a, st);
   if (e != cudaSuccess) return DCP_ERR_CUDA;
   if (plan.splits > 1) {
     const int64_t pairs = static_cast<int64_t>(D) * T * H;
@@ -181,6 +230,16 @@ dcp_status_t dcp_mla_decode_partial(const void* q, int64_t q_stride_tok, const v
     if (e != cudaSuccess) return DCP_ERR_CUDA;
   }
   return DCP_OK;
+}
+
+int32_t dcp_decode_kernel_launches(int32_t B, int32_t T, int32_t H, int32_t D, int32_t interleave,
+                                   int32_t max_seq_len, int32_t max_q_len, size_t workspace_bytes) {
+  if (B < 0 || T < 0 || H < 1 || H > 1024 || D < 1 || D > DCP_MAX_SHARDS || interleave < 1 || max_seq_len < 0 ||
+      max_q_len < 0)
+    return -1;
+  if (B == 0 || T == 0) return 0;
+  const DecodeLaunch L = decode_launch(T, H, D, interleave, max_seq_len, workspace_bytes > 0, workspace_bytes);
+  return 1 + (L.plan.splits > 1 ? 1 : 0) + (L.use_order ? 1 : 0);
 }
 
 dcp_status_t dcp_lse_combine(const float* O_part, const float* lse_part, const int32_t* seq_lens,

@@ -152,7 +152,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(DecodeArgs a) {
   const bool score = cta == 0;
   const uint32_t peer = cta ^ 1u;
 
-  const int64_t unit = blockIdx.x >> 1;
+  const int64_t unit = a.unit_order ? __ldg(a.unit_order + (blockIdx.x >> 1)) : (blockIdx.x >> 1);
   const int per_row = a.D * a.plan.splits;
   const int r = static_cast<int>(unit / per_row);
   const int d = static_cast<int>((unit % per_row) / a.plan.splits);
@@ -704,6 +704,55 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(DecodeArgs a) {
   }
 }
 
+// Launch order of the units (see launch_unit_order): one CTA; keys count
+// into 33 buckets, then a stable scatter in chunks of 1024 units (rank in the
+// warp by __match_any_sync, warps before this one by their bucket counts).
+__global__ void __launch_bounds__(1024) unit_order_kernel(DecodeArgs a, int32_t units, int32_t* order) {
+  __shared__ int32_t cnt[33], off[33];
+  __shared__ int32_t wcnt[32][33];
+  const int t = threadIdx.x, w = t >> 5, lane = t & 31;
+  auto key_of = [&](int32_t u) -> int {
+    const int per_row = a.D * a.plan.splits;
+    const int r = u / per_row, d = (u % per_row) / a.plan.splits, s = u % a.plan.splits;
+    const RowInfo ri = resolve_row(a.seq_lens, a.qsl, a.B, r, a.max_seq_len, a.max_q_len);
+    const int32_t n = ri.padding ? 0 : local_len(ri.L, d, a.D, a.I);
+    const int32_t lo = s * a.plan.chunk, hi = min(n, lo + a.plan.chunk);
+    const int32_t tiles = lo < hi ? (hi - lo + kTile - 1) / kTile : 0;
+    return tiles == 0 ? 0 : 32 - __clz(tiles);  // 1 + floor(log2 tiles)
+  };
+  if (t < 33) cnt[t] = 0;
+  __syncthreads();
+  for (int32_t u = t; u < units; u += 1024) atomicAdd(&cnt[key_of(u)], 1);
+  __syncthreads();
+  if (t == 0) {
+    int32_t acc = 0;
+    for (int k = 32; k >= 0; --k) { off[k] = acc; acc += cnt[k]; }
+  }
+  __syncthreads();
+  for (int32_t base = 0; base < units; base += 1024) {
+    for (int i = t; i < 32 * 33; i += 1024) (&wcnt[0][0])[i] = 0;
+    __syncthreads();
+    const int32_t u = base + t;
+    const int k = u < units ? key_of(u) : -1;
+    const unsigned same = __match_any_sync(0xffffffffu, k);
+    const int rank = __popc(same & ((1u << lane) - 1u));
+    if (k >= 0 && rank == 0) wcnt[w][k] = __popc(same);
+    __syncthreads();
+    if (k >= 0) {
+      int32_t pos = off[k] + rank;
+      for (int v = 0; v < w; ++v) pos += wcnt[v][k];
+      order[pos] = u;
+    }
+    __syncthreads();
+    if (t < 33) {
+      int32_t add = 0;
+      for (int v = 0; v < 32; ++v) add += wcnt[v][t];
+      off[t] += add;
+    }
+    __syncthreads();
+  }
+}
+
 cudaLaunchConfig_t launch_config(int64_t units, cudaStream_t st, cudaLaunchAttribute* attr) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(2 * units));
@@ -740,6 +789,12 @@ int decode_tc_resident_ctas() {
   cached_dev = dev;
   cached = 2 * clusters;
   return cached;
+}
+
+cudaError_t launch_unit_order(const DecodeArgs& a, int32_t units, int32_t* order, cudaStream_t st) {
+  if (units <= 0) return cudaSuccess;
+  unit_order_kernel<<<1, 1024, 0, st>>>(a, units, order);
+  return cudaGetLastError();
 }
 
 bool decode_tc_supported(const DecodeArgs& a) { return a.H <= 128 && (a.plan.chunk % kTile) == 0; }

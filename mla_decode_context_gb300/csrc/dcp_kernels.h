@@ -28,6 +28,9 @@ struct DecodeArgs {
   float* lse_dst;
   SplitPlan plan;
   int32_t* dev_error;
+  // Optional launch order of the tensor-core decode's units (cluster c runs
+  // unit unit_order[c]); nullptr = index order.
+  const int32_t* unit_order;
 };
 
 // Generic LSE merge over `nsrc` sources: pair p (flattened) reads
@@ -49,6 +52,11 @@ cudaError_t launch_decode_simt(const DecodeArgs& a, cudaStream_t st);
 // H <= 128 and the shard layout tiles into whole TMA boxes: block_size a
 // multiple of D * interleave (runs inside blocks) or interleave a multiple
 // of block_size (whole blocks per run).
+// Writes into `order` the units (row, shard, split) of `a` sorted by
+// decreasing 1 + floor(log2(tiles)), stable in unit index, so that long units
+// start first when there are more units than clusters that fit at once.
+cudaError_t launch_unit_order(const DecodeArgs& a, int32_t units, int32_t* order, cudaStream_t st);
+
 bool decode_tc_supported(const DecodeArgs& a);
 // CTAs of the tensor-core decode resident at once on the current device
 // (0 if unknown); the split plan sizes one wave from it.

@@ -66,10 +66,20 @@ def test_workspace_size(L):
     assert dcp.dcp_decode_workspace_size(0, 0, 128, 8, 1000, 1) == 0
     # long-context single request: split-KV needs a workspace
     assert dcp.dcp_decode_workspace_size(1, 1, 128, 8, 120000, 1) > 0
-    # many rows fill the GPU without splitting
-    assert dcp.dcp_decode_workspace_size(64, 64, 128, 8, 32768, 1) == 0
+    # many rows fill the GPU without splitting: only the units' launch order
+    # (one int32 per unit, rounded to 256 bytes)
+    assert dcp.dcp_decode_workspace_size(64, 64, 128, 8, 32768, 1) == 64 * 8 * 4
     with pytest.raises(dcp.DCPError):
         dcp.dcp_decode_workspace_size(1, 1, 128, 33, 100, 1)
+
+
+def test_kernel_launch_count(L):
+    assert dcp.dcp_decode_kernel_launches(0, 0, 128, 8, 1, 1000, 1, 0) == 0
+    # long-context single request: decode + split merge
+    ws = dcp.dcp_decode_workspace_size(1, 1, 128, 8, 120000, 1)
+    assert dcp.dcp_decode_kernel_launches(1, 1, 128, 8, 1, 120000, 1, ws) == 2
+    with pytest.raises(dcp.DCPError):
+        dcp.dcp_decode_kernel_launches(1, 1, 128, 33, 1, 100, 1, 0)
 
 
 def _decode(L, **kw):

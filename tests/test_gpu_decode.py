@@ -91,6 +91,33 @@ def test_strided_rows_match_dense():
     assert torch.equal(O, O2) and torch.equal(lse, lse2)
 
 
+def test_unit_order_does_not_change_results():
+    """More units than clusters (12 rows x 8 shards, unsplit): with the full
+    workspace the long units start first; with no workspace they start in
+    index order.  Every unit's arithmetic is its own, so the partials are
+    bit-identical either way."""
+    inp = wl.make_decode_inputs(SMALL[-1])
+    t = G.to_device(inp)
+    T, H = t["q"].shape[:2]
+    B, D, msl = inp["B"], inp["D"], max(1, inp["max_seq_len"])
+    ws_bytes = dcp.dcp_decode_workspace_size(B, T, H, D, msl, 1)
+    ordered = dcp.dcp_decode_kernel_launches(B, T, H, D, inp["interleave"], msl, 1, ws_bytes)
+    plain = dcp.dcp_decode_kernel_launches(B, T, H, D, inp["interleave"], msl, 1, 0)
+    assert ordered == plain + 1  # the ordering kernel runs only with room for the order
+    outs = []
+    for ws in (torch.empty(ws_bytes, dtype=torch.uint8, device="cuda"), None):
+        O = torch.empty((D, T, H, 512), dtype=torch.float32, device="cuda")
+        lse = torch.empty((D, T, H), dtype=torch.float32, device="cuda")
+        err = torch.zeros(1, dtype=torch.int32, device="cuda")
+        dcp.dcp_mla_decode_partial(t["q"], t["kv_cache"], t["block_table"], t["seq_lens"], t["query_start_loc"],
+                                   O, lse, D=D, interleave=inp["interleave"], scale=inp["scale"], max_seq_len=msl,
+                                   max_q_len=1, workspace=ws, dev_error=err)
+        torch.cuda.synchronize()
+        assert int(err.item()) == 0
+        outs.append((O, lse))
+    assert torch.equal(outs[0][0], outs[1][0]) and torch.equal(outs[0][1], outs[1][1])
+
+
 def test_empty_batch_is_a_noop():
     inp = wl.make_decode_inputs(wl.TINY)
     t = G.to_device(inp)
