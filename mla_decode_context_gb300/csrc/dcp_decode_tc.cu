@@ -4,10 +4,11 @@
 // row (the MMA M dimension) against the split's shard tokens, in tiles of 32
 // tokens.  A unit runs on a cluster of two CTAs with different jobs:
 //   score CTA (rank 0)  holds Q (128 x 576 bf16 = 288 TMEM columns), computes
-//                       S(j) = Q K(j)^T as two halves over dims [0, 288) and
-//                       [288, 576) (18 tcgen05.mma each, M=128 N=32 K=16, A
-//                       from TMEM, issued by two warps into two accumulators
-//                       that the softmax adds), runs the online softmax and
+//                       S(j) = Q K(j)^T as three thirds over dims [0, 192),
+//                       [192, 384), [384, 576) (12 tcgen05.mma each, M=128
+//                       N=32 K=16, A from TMEM, issued by three warps into
+//                       three accumulators that the softmax adds), runs the
+//                       online softmax and
 //                       ships P(j) (bf16, 8 KB) plus each head's running max
 //                       to the value CTA;
 //   value CTA (rank 1)  holds O (128 x 512 fp32 = all 512 TMEM columns),
@@ -40,8 +41,8 @@
 //   warps 0-3   score: Q load, then softmax group 0 (thread = head = TMEM
 //                      lane; even tiles)
 //               value: max tracking and O rescale; epilogue columns 0-255
-//   warps 4-9   score: (4-7 also Q load) S issuers: warp 4 + 2i + k issues
-//                      half k of S for tiles j = i mod 3 into S slot i (a
+//   warps 4-9   score: (4-7 also Q load) S issuers: warp 4 + 3i + k issues
+//                      third k of S for tiles j = i mod 2 into S slot i (a
 //                      tcgen05.mma holds its issuing thread far longer than
 //                      an N=32 product takes, so issue is spread over warps)
 //               value: 4-7 epilogue columns 256-511; 8 forwarder (own
@@ -73,7 +74,8 @@ constexpr int kGroupThreads = 32 * kProdWarps / 2;
 constexpr int kHalfBytes = 4 * kChunkBytes;      // 4 chunks: forwarded each way per tile
 constexpr int kOwn = 7;                          // value CTA: own ring slots (chunks 4-7)
 constexpr int kRecv = 4;                         // value CTA: receive ring slots (chunks 0-3)
-constexpr int kSBuf = 3;                         // S slots (two 32-column halves each) in TMEM
+constexpr int kSBuf = 2;                         // S slots (three 32-column thirds each) in TMEM
+constexpr int kSParts = 3;                       // K-parts of S, one issuing warp each
 constexpr int kPSlots = 4;                       // P slots in the value CTA
 constexpr int kPBytes = 128 * kTile * 2;         // P tile: 128 rows x 32 bf16, 64B-swizzled
 constexpr int kPWarpBytes = kPBytes / 4;         // one softmax warp's 32 rows
@@ -85,21 +87,22 @@ constexpr float kRescaleLog2 = 8.0f;
 
 // TMEM columns
 constexpr uint32_t kColQ = 0;    // score: 288 columns of Q, 2 bf16 per column
-constexpr uint32_t kColS = 288;  // score: 3 slots x 2 halves x 32 columns of S
+constexpr uint32_t kColS = 288;  // score: 2 slots x 3 thirds x 32 columns of S
 constexpr uint32_t kColO = 0;    // value: 512 columns of O
 constexpr uint32_t kTmemCols = 512;
 
 struct __align__(8) Bars {
   uint64_t kv_loaded[kStages];  // score: own rows of tile j landed (every thread of tile j's producer group)
   uint64_t kv_full[kStages];    // score: the value CTA's 16 KB of tile j landed (armed by a producer)
-  // s_done (both CTAs): the score CTA's stage of tile j is free again: both
-  // halves of S(j) done and tile j's V part has landed in the value CTA
+  // s_done (both CTAs): the score CTA's stage of tile j is free again: all
+  // three parts of S(j) done and chunks 0-3 of tile j have landed in the
+  // value CTA
   uint64_t s_done[kStages];
   uint64_t own_loaded[kOwn];    // value: rows of tile j in own slot j % kOwn (every thread of its producer group)
   uint64_t own_free[kOwn];      // value: PV(j) done with own slot j % kOwn
   uint64_t v_full[kRecv];       // value: chunks 0-3 of tile j landed in receive slot j % kRecv
   uint64_t v_free[kRecv];       // score (multicast commit of PV(j)): receive slot j % kRecv may refill
-  uint64_t s_full[kSBuf];     // score: both halves' commits + the slot's mask
+  uint64_t s_full[kSBuf];     // score: the three parts' commits + the slot's mask
   uint64_t s_free[kSBuf];     // score: the softmax has read the slot (4 warps)
   uint64_t q_staged;          // score: Q is in shared memory (threads of warps 0-7)
   uint64_t q_ready;           // score: Q is in TMEM and stages 0-3 are free again (warps 0-7)
@@ -110,7 +113,7 @@ struct __align__(8) Bars {
   uint64_t pv_done[kPSlots];  // value: PV(j) completes phase j / kPSlots of pv_done[j % kPSlots]
   uint64_t o_final;           // value: last PV complete
   uint64_t fin_l;             // value: 1/l of every head arrived from the score CTA
-  uint64_t fin[1 + 2 * kSBuf];  // each issuing warp's MMAs complete
+  uint64_t fin[1 + kSParts * kSBuf];  // each issuing warp's MMAs complete
   uint64_t m_pub[2];          // score: running max after tile j published (phase j / 2 of m_pub[j & 1]; 4 warps)
   uint64_t sm_fin;            // score: both softmax groups' final l and m written (8 warps)
   uint32_t mask[kStages];     // valid rows of the tile in each stage
@@ -187,11 +190,11 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(DecodeArgs a) {
     for (int i = 0; i < kStages; ++i) {
       mbar_init(&bar.kv_loaded[i], kGroupThreads);
       mbar_init(&bar.kv_full[i], 1);
-      mbar_init(&bar.s_done[i], 3);
+      mbar_init(&bar.s_done[i], kSParts + 1);
     }
     for (int i = 0; i < kOwn; ++i) { mbar_init(&bar.own_loaded[i], kGroupThreads); mbar_init(&bar.own_free[i], 1); }
     for (int i = 0; i < kRecv; ++i) { mbar_init(&bar.v_full[i], 1); mbar_init(&bar.v_free[i], 1); }
-    for (int i = 0; i < kSBuf; ++i) { mbar_init(&bar.s_full[i], 3); mbar_init(&bar.s_free[i], 4); }
+    for (int i = 0; i < kSBuf; ++i) { mbar_init(&bar.s_full[i], kSParts + 1); mbar_init(&bar.s_free[i], 4); }
     mbar_init(&bar.q_staged, 256);
     mbar_init(&bar.q_ready, 8);
     mbar_init(&bar.q_gone, 1);
@@ -203,7 +206,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(DecodeArgs a) {
     }
     mbar_init(&bar.o_final, 1);
     mbar_init(&bar.fin_l, 1);
-    for (int i = 0; i < 1 + 2 * kSBuf; ++i) mbar_init(&bar.fin[i], 1);
+    for (int i = 0; i < 1 + kSParts * kSBuf; ++i) mbar_init(&bar.fin[i], 1);
     mbar_init(&bar.m_pub[0], 4);
     mbar_init(&bar.m_pub[1], 4);
     mbar_init(&bar.sm_fin, 8);
@@ -394,18 +397,18 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(DecodeArgs a) {
     if (!ok) set_abort(bar, a.dev_error);
   } else if (score && warp >= 4 && warp < 10) {
     // ------------------------------------------------------- S MMA issuers
-    // warp 4 + 2b + half owns half `half` of S slot b (dims [288 half,
-    // 288 half + 288): 18 k-steps) for tiles j = b (mod 3).  Stage layout:
+    // warp 4 + 3b + part owns third `part` of S slot b (dims [192 part,
+    // 192 part + 192): 12 k-steps) for tiles j = b (mod 2).  Stage layout:
     // chunk-major, 4 KB per 64-dim chunk, 8-row groups 1 KB apart.
-    const int b = (warp - 4) >> 1, half = (warp - 4) & 1;
+    const int b = (warp - 4) / kSParts, part = (warp - 4) % kSParts;
     const uint32_t id_s = idesc_bf16(128, kTile, 0, 0);
     const uint64_t dk = smem_desc(smem_base + kOffStages, 16, 1024, kSwizzle128B);
-    const uint32_t dS = tbase + kColS + 64 * b + 32 * half;
+    const uint32_t dS = tbase + kColS + 96 * b + 32 * part;
     bool ok = __all_sync(0xffffffffu, mbar_wait(&bar.q_ready, 0));
     tc_fence_after();
     for (int j = b; ok && j < ntiles; j += kSBuf) {
       const int st = j % kStages, u = j / kSBuf;
-      // s_free first: once the softmax has read S(j - 3) it has read every
+      // s_free first: once the softmax has read S(j - 2) it has read every
       // earlier tile, so the stage's previous fill (tile j - 5) is consumed
       // and the kv_loaded / kv_full parities below can only mean tile j
       ok = __all_sync(0xffffffffu, mbar_wait(&bar.s_free[b], (u & 1) ^ 1) &&
@@ -415,7 +418,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(DecodeArgs a) {
       // rows that were not loaded are zero and only reach S columns the
       // softmax masks; the stage's mask travels with the S slot, since the
       // stage itself is refilled as soon as both halves of S are done
-      if (half == 0 && lane == 0) {
+      if (part == 0 && lane == 0) {
         bar.smask[b] = bar.mask[st];
         mbar_arrive(&bar.s_full[b]);
       }
@@ -424,8 +427,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(DecodeArgs a) {
       if (lane == 0) {
         const uint64_t so = static_cast<uint64_t>((st * kStageBytes) >> 4);
 #pragma unroll 6
-        for (int i = 0; i < 18; ++i) {
-          const int k = 18 * half + i;
+        for (int i = 0; i < 12; ++i) {
+          const int k = 12 * part + i;
           mma_ts(dS, tbase + kColQ + 8 * k, dk + so + (((k >> 2) * kChunkBytes + (k & 3) * 32) >> 4), id_s, i > 0);
         }
         mma_commit(&bar.s_full[b]);
@@ -434,9 +437,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(DecodeArgs a) {
       __syncwarp();
     }
     if (!ok) set_abort(bar, a.dev_error);
-    if (lane == 0) mma_commit(&bar.fin[1 + 2 * b + half]);
+    if (lane == 0) mma_commit(&bar.fin[1 + kSParts * b + part]);
     __syncwarp();
-    mbar_wait(&bar.fin[1 + 2 * b + half], 0);
+    mbar_wait(&bar.fin[1 + kSParts * b + part], 0);
   } else if (score && (warp < 4 || warp >= kSmWarp1)) {
     // ------------------------------------------------------------- softmax
     // Two groups of four warps take alternate tiles.  The running max per
@@ -460,16 +463,26 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(DecodeArgs a) {
       if (!ok) break;
       tc_fence_after();
       uint32_t sr[32], sr2[32];
-      tmem_ld32(lane_addr + kColS + 64 * b, sr);
-      tmem_ld32(lane_addr + kColS + 64 * b + 32, sr2);
+      tmem_ld32(lane_addr + kColS + 96 * b, sr);
+      tmem_ld32(lane_addr + kColS + 96 * b + 32, sr2);
       const uint32_t mask = *reinterpret_cast<volatile uint32_t*>(&bar.smask[b]);
+      tmem_wait_ld();
+      float sc[32];
+#pragma unroll
+      for (int i = 0; i < 16; ++i)  // the K-parts of S, pairwise
+        f2_unpack(f2_add(f2_pack(__uint_as_float(sr[2 * i]), __uint_as_float(sr[2 * i + 1])),
+                         f2_pack(__uint_as_float(sr2[2 * i]), __uint_as_float(sr2[2 * i + 1]))),
+                  sc[2 * i], sc[2 * i + 1]);
+      tmem_ld32(lane_addr + kColS + 96 * b + 64, sr);
       tmem_wait_ld();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bar.s_free[b]);
-      float sc[32];
 #pragma unroll
-      for (int i = 0; i < 32; ++i) sc[i] = __uint_as_float(sr[i]) + __uint_as_float(sr2[i]);
+      for (int i = 0; i < 16; ++i)
+        f2_unpack(f2_add(f2_pack(sc[2 * i], sc[2 * i + 1]),
+                         f2_pack(__uint_as_float(sr[2 * i]), __uint_as_float(sr[2 * i + 1]))),
+                  sc[2 * i], sc[2 * i + 1]);
       // online softmax (base 2); masked tokens get weight 0 by selection
       if (mask != 0xffffffffu) {
 #pragma unroll
@@ -504,17 +517,22 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(DecodeArgs a) {
       // p = 2^(s * scale * log2e - m); masked (-inf) scores give exactly 0,
       // and nothing is live while m is still -inf
       const float nm = m_used == -INFINITY ? 0.f : -m_used;
+      const uint64_t sl2x2 = f2_pack(sl2, sl2), nmx2 = f2_pack(nm, nm);
       uint32_t pk[16];
-      float ps[4] = {0.f, 0.f, 0.f, 0.f};
+      uint64_t ps[2] = {f2_pack(0.f, 0.f), f2_pack(0.f, 0.f)};
 #pragma unroll
       for (int i = 0; i < 16; ++i) {
-        const float p0 = ex2_approx(fmaf(sc[2 * i], sl2, nm));
-        const float p1 = ex2_approx(fmaf(sc[2 * i + 1], sl2, nm));
+        float e0, e1;
+        f2_unpack(f2_fma(f2_pack(sc[2 * i], sc[2 * i + 1]), sl2x2, nmx2), e0, e1);
+        const float p0 = ex2_approx(e0), p1 = ex2_approx(e1);
         __nv_bfloat162 pb = __floats2bfloat162_rn(p0, p1);  // P feeds the PV MMA in bf16
-        ps[i & 3] += p0 + p1;                                // l (hence the LSE) stays fp32
+        ps[i & 1] = f2_add(ps[i & 1], f2_pack(p0, p1));     // l (hence the LSE) stays fp32
         pk[i] = *reinterpret_cast<uint32_t*>(&pb);
       }
-      l_sum += (ps[0] + ps[1]) + (ps[2] + ps[3]);
+      float q0, q1, q2, q3;
+      f2_unpack(ps[0], q0, q1);
+      f2_unpack(ps[1], q2, q3);
+      l_sum += (q0 + q1) + (q2 + q3);
       // the slot (and this CTA's staging copy of it) is free once PV(j - kPSlots) is done
       ok = __all_sync(0xffffffffu, mbar_wait_cluster(&bar.p_free[slot], ((j / kPSlots) & 1) ^ 1));
       if (!ok) break;
