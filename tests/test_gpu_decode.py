@@ -29,6 +29,13 @@ SMALL = [
                   interleave=1),
     wl.DecodeSpec("h128_long_split", seed=38, B=1, seq_lens=(9000,), H=128, block_size=64, D=8,
                   interleave=1),
+    # the largest shard count (32); 64-token blocks hold two tokens per shard
+    wl.DecodeSpec("h128_d32_i1_max_shards", seed=40, B=2, seq_lens=(5000, 700), H=128, block_size=64,
+                  D=32, interleave=1),
+    # more heads than the tensor-core kernel takes: the CUDA-core kernel runs
+    # under both parametrisations
+    wl.DecodeSpec("h256_d4_i2_wide_heads", seed=41, B=2, seq_lens=(300, 1000), H=256, block_size=16, D=4,
+                  interleave=2),
     # more units than clusters, so one split per shard: 20-25 tiles per unit
     # (every stage, S buffer and P slot reused several times)
     wl.DecodeSpec("h128_b12_unsplit", seed=39, B=12,
