@@ -25,11 +25,19 @@
 // token per row, straight into the 128B-swizzled chunk-major layout the MMAs
 // read.  Each CTA forwards the 16 KB its peer lacks with one DSMEM bulk copy:
 // value -> score chunks 4-7 (into the stage, which then holds the whole tile
-// for S), score -> value chunks 0-3 (into a 3-slot receive ring; PV reads V
-// from the receive slot and the own slot).  The own ring is 8 deep, so the
-// loop through PV that feeds back into the loads (and through them into S)
-// spans 8 tiles.  A DSMEM copy was measured at ~900 cycles of round trip plus
-// ~47 cycles per KB, so each direction carries at most 24 KB per tile.
+// for S), score -> value chunks 0-3 (into a 4-slot receive ring; PV reads V
+// from the receive slot and the own slot).  A DSMEM copy was measured at
+// ~900 cycles of round trip plus ~47 cycles per KB, so each direction carries
+// at most 24 KB per tile.
+//
+// While an SM streams cp.async, its shared-memory loads, proxy fences and
+// st.async take ~500 cycles each and a release-ordered remote arrival
+// thousands, whereas mbarrier waits, local arrivals, bulk copies and tcgen05
+// operations stay at tens of cycles (measured on GB300).  So every per-tile
+// loop below is built from the cheap kind: one warp fences a ring slot and
+// arrives on the barrier its consumers wait on, the slot-consumed signal
+// across the cluster is a relaxed arrival, P and the running max travel by
+// bulk copy, and the softmax groups share their maxima without waiting.
 // Row-by-row addressing takes any paging geometry (block size, shard count,
 // interleave); rows that must not be read (past the split, bad block ids)
 // are zero-filled.  (TMA boxes were measured to cost a few hundred cycles
@@ -46,9 +54,11 @@
 //                      tcgen05.mma holds its issuing thread far longer than
 //                      an N=32 product takes, so issue is spread over warps)
 //               value: 4-7 epilogue columns 256-511; 8 forwarder (own
-//                      ring -> score stage); 9 receive-ring arrivals
-//   warp 10     both:  TMEM allocation; score: forwarder (stage -> receive
-//                      ring); value: PV issuer
+//                      ring -> score stage); 9 receive-ring arrivals and
+//                      the own slot's proxy fence for PV
+//   warp 10     both:  TMEM allocation; score: proxy fence of the stage's
+//                      own rows, forwarder (stage -> receive ring); value:
+//                      PV issuer
 //   warps 11-18 both:  producers (cp.async; the score CTA's wait until Q has
 //                      left stages 0-3 for TMEM)
 //   warps 19-22 score: softmax group 1 (odd tiles)
@@ -93,7 +103,10 @@ constexpr uint32_t kTmemCols = 512;
 
 struct __align__(8) Bars {
   uint64_t kv_loaded[kStages];  // score: own rows of tile j landed (every thread of tile j's producer group)
-  uint64_t kv_full[kStages];    // score: the value CTA's 16 KB of tile j landed (armed by a producer)
+  // kv_full (score): the whole tile j is in its stage for S: the value CTA's
+  // 16 KB landed (armed by a producer) and the forwarder has made this CTA's
+  // own rows visible to the tensor cores
+  uint64_t kv_full[kStages];
   // s_done (both CTAs): the score CTA's stage of tile j is free again: all
   // three parts of S(j) done and chunks 0-3 of tile j have landed in the
   // value CTA
@@ -102,22 +115,28 @@ struct __align__(8) Bars {
   uint64_t own_free[kOwn];      // value: PV(j) done with own slot j % kOwn
   uint64_t v_full[kRecv];       // value: chunks 0-3 of tile j landed in receive slot j % kRecv
   uint64_t v_free[kRecv];       // score (multicast commit of PV(j)): receive slot j % kRecv may refill
-  uint64_t s_full[kSBuf];     // score: the three parts' commits + the slot's mask
+  uint64_t s_full[kSBuf];     // score: the three parts' commits + part 0's arrival
   uint64_t s_free[kSBuf];     // score: the softmax has read the slot (4 warps)
   uint64_t q_staged;          // score: Q is in shared memory (threads of warps 0-7)
   uint64_t q_ready;           // score: Q is in TMEM and stages 0-3 are free again (warps 0-7)
   uint64_t q_gone;            // value: the score CTA's stages no longer hold Q (remote arrival)
   uint64_t p_full[kPSlots];   // value: P(j) and the max of tile j arrived
   uint64_t p_free[kPSlots];   // both (multicast commit of PV(j)); the score CTA waits on it
-  uint64_t p_ok[kPSlots];     // value: max checked, O rescaled if needed (4 warps)
+  // p_ok (value): PV(j) may go: the max is checked and O rescaled if needed
+  // (4 warps), and both halves of V(j) are visible to the tensor cores (the
+  // receive-ring warp)
+  uint64_t p_ok[kPSlots];
   uint64_t pv_done[kPSlots];  // value: PV(j) completes phase j / kPSlots of pv_done[j % kPSlots]
   uint64_t o_final;           // value: last PV complete
   uint64_t fin_l;             // value: 1/l of every head arrived from the score CTA
   uint64_t fin[1 + kSParts * kSBuf];  // each issuing warp's MMAs complete
-  uint64_t m_pub[2];          // score: running max after tile j published (phase j / 2 of m_pub[j & 1]; 4 warps)
+  uint64_t m_pub[8];          // score: running max after tile j posted (phase j / 8 of m_pub[j % 8]; 4 warps)
   uint64_t sm_fin;            // score: both softmax groups' final l and m written (8 warps)
-  uint32_t mask[kStages];     // valid rows of the tile in each stage
-  uint32_t smask[kSBuf];      // score: valid rows of the tile in each S slot
+  // score: valid rows of tile j in mask[j % 16] (written by the producer
+  // before it arms kv_full; the slot is rewritten 16 tiles later, long after
+  // the softmax of tile j has read it: a producer nine or more tiles ahead
+  // needs PV(j), hence P(j), done)
+  uint32_t mask[16];
   uint32_t tmem;
   int32_t abort;
 };
@@ -127,8 +146,8 @@ constexpr int kOffOwn = 0;                               // value: own ring
 constexpr int kOffRecv = kOwn * kHalfBytes;              // value: receive ring
 constexpr int kOffP = kStages * kStageBytes;             // value: P slots; score: P staging
 constexpr int kOffFin = kOffP + kPSlots * kPSlotBytes;   // value: 1/l per head
-constexpr int kOffSm = kOffFin + 512;                    // score: softmax group hand-off
-constexpr int kOffBars = kOffSm + 5 * 128 * 4;
+constexpr int kOffSm = kOffFin + 512;                    // score: running max per tile (8 x 128), final l, m
+constexpr int kOffBars = kOffSm + 12 * 128 * 4;
 constexpr int kSmemBytes = kOffBars + static_cast<int>(sizeof(Bars)) + 1024;  // + alignment slack
 static_assert(kSmemBytes <= 232448, "exceeds the 227 KB of shared memory per CTA");
 static_assert(kPSlotBytes % 1024 == 0 && kOffP % 1024 == 0, "P tiles must sit on swizzle-atom boundaries");
@@ -189,7 +208,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(DecodeArgs a) {
   if (threadIdx.x == 0) {
     for (int i = 0; i < kStages; ++i) {
       mbar_init(&bar.kv_loaded[i], kGroupThreads);
-      mbar_init(&bar.kv_full[i], 1);
+      mbar_init(&bar.kv_full[i], 2);
       mbar_init(&bar.s_done[i], kSParts + 1);
     }
     for (int i = 0; i < kOwn; ++i) { mbar_init(&bar.own_loaded[i], kGroupThreads); mbar_init(&bar.own_free[i], 1); }
@@ -201,14 +220,13 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(DecodeArgs a) {
     for (int i = 0; i < kPSlots; ++i) {
       mbar_init(&bar.p_full[i], 1);
       mbar_init(&bar.p_free[i], 1);
-      mbar_init(&bar.p_ok[i], 4);
+      mbar_init(&bar.p_ok[i], 5);
       mbar_init(&bar.pv_done[i], 1);
     }
     mbar_init(&bar.o_final, 1);
     mbar_init(&bar.fin_l, 1);
     for (int i = 0; i < 1 + kSParts * kSBuf; ++i) mbar_init(&bar.fin[i], 1);
-    mbar_init(&bar.m_pub[0], 4);
-    mbar_init(&bar.m_pub[1], 4);
+    for (int i = 0; i < 8; ++i) mbar_init(&bar.m_pub[i], 4);
     mbar_init(&bar.sm_fin, 8);
     bar.abort = 0;
     fence_mbar_init();
@@ -311,16 +329,18 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(DecodeArgs a) {
       const int32_t pos = pos_n, blk = blk_n;
       if (j + 2 < ntiles) fetch(j + 2);
       const int st = j % nslots;
+      // the abort flag is read here and tested after this tile's copies are
+      // issued, so that its shared-memory latency overlaps them
+      const bool ab = aborted(bar);
       ok = __all_sync(0xffffffffu, mbar_wait(&own_free[st], ((j / nslots) & 1) ^ 1));
-      if (ok) ok = !__any_sync(0xffffffffu, aborted(bar));
       if (!ok) break;
       const bool valid = in && blk >= 0 && blk < a.num_blocks;
       if (in && !valid && score && leader) report(a.dev_error, DCP_DEVERR_BAD_BLOCK);
-      const int64_t roff =
-          valid ? (static_cast<int64_t>(blk) * a.block_size + pos % a.block_size) * (kKDim * 2) : 0;
+      // cache row (fits in 31 bits: the library only takes caches of < 2^31 rows)
+      const int32_t crow = valid ? blk * a.block_size + pos % a.block_size : 0;
       const uint32_t mask = __ballot_sync(0xffffffffu, valid);
       if (score && leader && lane == 0) {
-        bar.mask[st] = mask;
+        bar.mask[j & 15] = mask;
         // tile j - 5 is done with the stage, so kv_full's previous phase is
         // complete: arm it for the value CTA's 16 KB of tile j
         mbar_arrive_expect_tx(&bar.kv_full[st], kHalfBytes);
@@ -334,27 +354,36 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(DecodeArgs a) {
         const int row = score ? p / 40 : p >> 5;
         const int u = p - row * upr;
         const int c = score ? (u < 32 ? (u >> 3) : 8) : 4 + (u >> 3);  // chunk
-        const int64_t ro = __shfl_sync(0xffffffffu, roff, row);
+        const int64_t ro = static_cast<int64_t>(__shfl_sync(0xffffffffu, crow, row)) * (kKDim * 2);
         const uint32_t dst = sbase + c * kChunkBytes + row * 128 + (((u & 7) ^ (row & 7)) << 4);
         cp_async16_zfill(dst, kvb + ro + c * 128 + (u & 7) * 16, ((mask >> row) & 1u) ? 16u : 0u);
       }
       cp_async_mbar_arrive_noinc(&own_loaded[st]);
+      if (__any_sync(0xffffffffu, ab)) {
+        ok = false;
+        break;
+      }
     }
     if (!ok) set_abort(bar, a.dev_error);
     cp_async_wait<0>();
   } else if (score && warp == 10) {
     // ------------------------------------------------- score CTA forwarder
-    // Once this CTA's own rows of tile j have landed and the value CTA's
-    // receive slot is free, copy chunks 0-3 (16 KB) into it.
+    // Once this CTA's own rows of tile j have landed, make them visible to
+    // the async proxy (one proxy fence here serves the S issuers too, through
+    // kv_full); once the value CTA's receive slot is free, copy chunks 0-3
+    // (16 KB) into it.
     bool ok = __all_sync(0xffffffffu, mbar_wait(&bar.q_ready, 0));
     // the value CTA's forwards into the stages (which held Q) may start
     if (ok && lane == 0) mbar_arrive_remote(map_peer(smem_u32(&bar.q_gone), peer));
     for (int j = 0; j < ntiles && ok; ++j) {
       const int st = j % kStages, rs = j % kRecv;
-      ok = __all_sync(0xffffffffu, mbar_wait(&bar.kv_loaded[st], (j / kStages) & 1) &&
-                                       mbar_wait_cluster(&bar.v_free[rs], ((j / kRecv) & 1) ^ 1));
+      ok = __all_sync(0xffffffffu, mbar_wait(&bar.kv_loaded[st], (j / kStages) & 1));
       if (!ok) break;
-      fence_proxy_async_smem();  // the producers' cp.async writes -> the bulk copy
+      fence_proxy_async_smem();  // the producers' cp.async writes -> S and the bulk copy
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bar.kv_full[st]);
+      ok = __all_sync(0xffffffffu, mbar_wait_cluster(&bar.v_free[rs], ((j / kRecv) & 1) ^ 1));
+      if (!ok) break;
       if (lane == 0)
         bulk_copy_to_peer(map_peer(smem_base + kOffRecv + rs * kHalfBytes, peer), smem + kOffStages + st * kStageBytes,
                           kHalfBytes, map_peer(smem_u32(&bar.v_full[rs]), peer));
@@ -382,17 +411,27 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(DecodeArgs a) {
     // ------------------------------------------------- receive-ring arrivals
     // When tile j's chunks 0-3 land, re-arm the slot for tile j + kRecv (that
     // fill needs PV(j) first, so it cannot complete before this) and tell
-    // both CTAs that the score CTA's stage of tile j has been read.
+    // both CTAs that the score CTA's stage of tile j has been read (a relaxed
+    // arrival: the copy's reads are complete, and nothing written here needs
+    // publishing).  Then, once this CTA's own rows of tile j have landed,
+    // fence them into the async proxy and let PV(j) go.  (This warp's arrival
+    // for tile j + kPSlots needs v_full(j + kPSlots), hence PV(j) done, so it
+    // cannot land in tile j's phase of p_ok.)
     bool ok = true;
     for (int j = 0; j < ntiles && ok; ++j) {
-      const int st = j % kStages, vs = j % kRecv;
+      const int st = j % kStages, vs = j % kRecv, os = j % kOwn;
       ok = __all_sync(0xffffffffu, mbar_wait_cluster(&bar.v_full[vs], (j / kRecv) & 1));
-      if (ok && lane == 0) {
+      if (!ok) break;
+      if (lane == 0) {
         mbar_arrive_expect_tx(&bar.v_full[vs], kHalfBytes);
         mbar_arrive(&bar.s_done[st]);
-        mbar_arrive_remote(map_peer(smem_u32(&bar.s_done[st]), peer));
+        mbar_arrive_remote_relaxed(map_peer(smem_u32(&bar.s_done[st]), peer));
       }
+      ok = __all_sync(0xffffffffu, mbar_wait(&bar.own_loaded[os], (j / kOwn) & 1));
+      if (!ok) break;
+      fence_proxy_async_smem();  // the own slot's cp.async rows -> PV
       __syncwarp();
+      if (lane == 0) mbar_arrive(&bar.p_ok[j % kPSlots]);
     }
     if (!ok) set_abort(bar, a.dev_error);
   } else if (score && warp >= 4 && warp < 10) {
@@ -410,19 +449,17 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(DecodeArgs a) {
       const int st = j % kStages, u = j / kSBuf;
       // s_free first: once the softmax has read S(j - 2) it has read every
       // earlier tile, so the stage's previous fill (tile j - 5) is consumed
-      // and the kv_loaded / kv_full parities below can only mean tile j
+      // and the kv_full parity below can only mean tile j.  kv_full covers
+      // both halves of the tile, this CTA's already fenced into the async
+      // proxy by the forwarder.
       ok = __all_sync(0xffffffffu, mbar_wait(&bar.s_free[b], (u & 1) ^ 1) &&
-                                       mbar_wait(&bar.kv_loaded[st], (j / kStages) & 1) &&
                                        mbar_wait_cluster(&bar.kv_full[st], (j / kStages) & 1));
       if (!ok) break;
       // rows that were not loaded are zero and only reach S columns the
-      // softmax masks; the stage's mask travels with the S slot, since the
-      // stage itself is refilled as soon as both halves of S are done
-      if (part == 0 && lane == 0) {
-        bar.smask[b] = bar.mask[st];
-        mbar_arrive(&bar.s_full[b]);
-      }
-      fence_proxy_async_smem();
+      // softmax masks.  Part 0's arrival passes on (release after the
+      // acquire of kv_full) the producer's write of the tile's mask, which
+      // the softmax reads after s_full.
+      if (part == 0 && lane == 0) mbar_arrive(&bar.s_full[b]);
       tc_fence_after();
       if (lane == 0) {
         const uint64_t so = static_cast<uint64_t>((st * kStageBytes) >> 4);
@@ -442,16 +479,22 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(DecodeArgs a) {
     mbar_wait(&bar.fin[1 + kSParts * b + part], 0);
   } else if (score && (warp < 4 || warp >= kSmWarp1)) {
     // ------------------------------------------------------------- softmax
-    // Two groups of four warps take alternate tiles.  The running max per
-    // head passes from tile to tile through shared memory (m_sh, published
-    // on m_pub); each group keeps the normaliser of its own tiles and
-    // rescales it whenever it learns of a new max.  The two normalisers are
-    // added at the end.
+    // Two groups of four warps take alternate tiles.  Each group keeps its
+    // own running max m and the normaliser of its own tiles in that max's
+    // scale.  After each tile a group posts its m (m_ring, m_pub), and before
+    // tile j it adopts, if larger, the other group's m after tile j - 3 (after
+    // tile 0 for tile 1): a lag at which the post is nearly always there
+    // already, so neither group waits on the other, and a fixed one, so the
+    // result does not depend on timing.  P(j) goes out with the m it was
+    // computed with; the value CTA rescales O whenever consecutive tiles' m
+    // differ, which happens only around the rare growth of the max (lazy by
+    // 2^8).  At the end the two normalisers are brought to the scale of O,
+    // which is the m of the last tile that had one.
     const int sg = warp < 4 ? 0 : 1, q4 = warp & 3;
     const int h = q4 * 32 + lane;
     const uint32_t lane_addr = tbase + (static_cast<uint32_t>(q4 * 32) << 16);
-    float* m_sh = reinterpret_cast<float*>(smem + kOffSm);  // [128]: running max after the latest tile
-    float* fin_sh = m_sh + 128;                             // [group][l, m][128]
+    float* m_ring = reinterpret_cast<float*>(smem + kOffSm);  // [tile % 8][128]: running max after the tile
+    float* fin_sh = m_ring + 8 * 128;                         // [group][l, m][128]
     const float sl2 = a.scale * kLog2e;
     float m_used = -INFINITY, l_sum = 0.f;
     const int sw = (h >> 1) & 3;  // 64-byte swizzle of row h
@@ -459,13 +502,23 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(DecodeArgs a) {
     bool ok = true;
     for (int j = sg; j < ntiles; j += 2) {
       const int b = j % kSBuf, slot = j % kPSlots;
+      // the other group's m after tile k, read early so that the load's
+      // latency overlaps the wait for S.  Slot k % 8 is posted again at tile
+      // k + 8, which needs PV(j) (through the P slots), so not before this read.
+      float m_other = -INFINITY;
+      const int k = j == 1 ? 0 : j - 3;
+      if (k >= 0) {
+        ok = __all_sync(0xffffffffu, mbar_wait(&bar.m_pub[k & 7], (k >> 3) & 1));
+        if (!ok) break;
+        m_other = *reinterpret_cast<volatile float*>(&m_ring[(k & 7) * 128 + h]);
+      }
       ok = __all_sync(0xffffffffu, mbar_wait(&bar.s_full[b], (j / kSBuf) & 1));
       if (!ok) break;
       tc_fence_after();
+      const uint32_t mask = *reinterpret_cast<volatile uint32_t*>(&bar.mask[j & 15]);
       uint32_t sr[32], sr2[32];
       tmem_ld32(lane_addr + kColS + 96 * b, sr);
       tmem_ld32(lane_addr + kColS + 96 * b + 32, sr2);
-      const uint32_t mask = *reinterpret_cast<volatile uint32_t*>(&bar.smask[b]);
       tmem_wait_ld();
       float sc[32];
 #pragma unroll
@@ -494,15 +547,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(DecodeArgs a) {
       for (int i = 0; i < 8; ++i) mx[i] = fmaxf(fmaxf(sc[4 * i], sc[4 * i + 1]), fmaxf(sc[4 * i + 2], sc[4 * i + 3]));
       const float tmax = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
                                fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))) * sl2;
-      if (j > 0) {
-        // the running max after tile j - 1 (the other group's); it only grows
-        ok = __all_sync(0xffffffffu, mbar_wait(&bar.m_pub[(j - 1) & 1], ((j - 1) >> 1) & 1));
-        if (!ok) break;
-        const float m_prev = *reinterpret_cast<volatile float*>(&m_sh[h]);
-        if (m_prev != m_used) {
-          if (m_used != -INFINITY) l_sum *= ex2_approx(m_used - m_prev);
-          m_used = m_prev;
-        }
+      // adopt the other group's max if it is larger (it only grows)
+      if (m_other > m_used) {
+        if (m_used != -INFINITY) l_sum *= ex2_approx(m_used - m_other);
+        m_used = m_other;
       }
       // lazy rescale: the running max only moves when it would grow by more
       // than 2^8 (the value CTA rescales O by the same factor)
@@ -511,9 +559,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(DecodeArgs a) {
         if (m_used != -INFINITY) l_sum *= ex2_approx(m_used - tmax);
         m_used = tmax;
       }
-      m_sh[h] = m_used;
+      m_ring[(j & 7) * 128 + h] = m_used;
       __syncwarp();
-      if (lane == 0) mbar_arrive(&bar.m_pub[j & 1]);
+      if (lane == 0) mbar_arrive(&bar.m_pub[j & 7]);
       // p = 2^(s * scale * log2e - m); masked (-inf) scores give exactly 0,
       // and nothing is live while m is still -inf
       const float nm = m_used == -INFINITY ? 0.f : -m_used;
@@ -541,13 +589,16 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(DecodeArgs a) {
       for (int c = 0; c < 4; ++c)
         *reinterpret_cast<uint4*>(stg + p_row + ((c ^ sw) << 4)) =
             make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+      *reinterpret_cast<float*>(stg + kPBytes + 4 * h) = m_used;
       fence_proxy_async_smem();
       __syncwarp();
-      const uint32_t peer_slot = map_peer(smem_base + kOffP + slot * kPSlotBytes, peer);
-      const uint32_t peer_full = map_peer(smem_u32(&bar.p_full[slot]), peer);
-      if (lane == 0)
+      if (lane == 0) {
+        // this warp's 32 rows of P, then its 32 maxima: two bulk copies
+        const uint32_t peer_slot = map_peer(smem_base + kOffP + slot * kPSlotBytes, peer);
+        const uint32_t peer_full = map_peer(smem_u32(&bar.p_full[slot]), peer);
         bulk_copy_to_peer(peer_slot + q4 * kPWarpBytes, stg + q4 * kPWarpBytes, kPWarpBytes, peer_full);
-      st_async_peer_b32(peer_slot + kPBytes + 4 * h, __float_as_uint(m_used), peer_full);
+        bulk_copy_to_peer(peer_slot + kPBytes + q4 * 128, stg + kPBytes + q4 * 128, 128, peer_full);
+      }
     }
     // both groups' normalisers meet here; group 0 finishes the unit
     fin_sh[(2 * sg) * 128 + h] = l_sum;
@@ -563,14 +614,19 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(DecodeArgs a) {
       } else {
         const float l1 = *reinterpret_cast<volatile float*>(&fin_sh[2 * 128 + h]);
         const float m1 = *reinterpret_cast<volatile float*>(&fin_sh[3 * 128 + h]);
-        const float mf = fmaxf(m_used, m1);  // the running max after the last tile
+        // O is in the scale of the m sent with the last tile that had one
+        // (a group's m is final after its last tile and never returns to
+        // -inf): the group of tile ntiles - 1, else the other group
+        const bool last0 = ((ntiles - 1) & 1) == 0;
+        float mo = last0 ? m_used : m1;
+        if (mo == -INFINITY) mo = last0 ? m1 : m_used;
         float l = 0.f;
-        if (m_used != -INFINITY) l += l_sum * ex2_approx(m_used - mf);
-        if (m1 != -INFINITY) l += l1 * ex2_approx(m1 - mf);
+        if (m_used != -INFINITY) l += l_sum * ex2_approx(m_used - mo);
+        if (m1 != -INFINITY) l += l1 * ex2_approx(m1 - mo);
         const bool live = l > 0.f;
         st_async_peer_b32(map_peer(smem_base + kOffFin + 4 * h, peer), __float_as_uint(live ? 1.f / l : 0.f),
                           map_peer(smem_u32(&bar.fin_l), peer));
-        if (h < a.H) a.lse_dst[pair0 + h] = live ? (mf + log2f(l)) * kLn2 : -INFINITY;
+        if (h < a.H) a.lse_dst[pair0 + h] = live ? (mo + log2f(l)) * kLn2 : -INFINITY;
       }
     }
   } else if (!score && warp == 10) {
@@ -584,18 +640,14 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(DecodeArgs a) {
     const uint32_t id_o = idesc_bf16(128, 256, 0, 1);
     const uint64_t dv = smem_desc(smem_base, kChunkBytes, 1024, kSwizzle128B);
     const uint64_t dp = smem_desc(smem_base + kOffP, 16, 512, kSwizzle64B);
+    // p_ok(j) stands for everything PV(j) needs: P(j) arrived and O rescaled
+    // (warps 0-3, which saw p_full(j)), V(j)'s receive half landed and its
+    // own half fenced into the async proxy (warp 9).
     bool ok = true;
     for (int j = 0; j < ntiles; ++j) {
       const int vs = j % kRecv, os = j % kOwn, slot = j % kPSlots;
-      ok = __all_sync(0xffffffffu, mbar_wait(&bar.p_ok[slot], (j / kPSlots) & 1) &&
-                                       mbar_wait_cluster(&bar.p_full[slot], (j / kPSlots) & 1) &&
-                                       mbar_wait_cluster(&bar.v_full[vs], (j / kRecv) & 1) &&
-                                       mbar_wait(&bar.own_loaded[os], (j / kOwn) & 1));
+      ok = __all_sync(0xffffffffu, mbar_wait(&bar.p_ok[slot], (j / kPSlots) & 1));
       if (!ok) break;
-      // the slot's next fill (tile j + kPSlots) cannot start before PV(j)
-      // frees it, i.e. after this arm
-      if (lane == 0) mbar_arrive_expect_tx(&bar.p_full[slot], kPTx);
-      fence_proxy_async_smem();
       tc_fence_after();
       if (lane == 0) {
         const uint64_t sv[2] = {static_cast<uint64_t>((kOffRecv + vs * kHalfBytes) >> 4),
@@ -631,9 +683,13 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(DecodeArgs a) {
         const int slot = j % kPSlots;
         ok = __all_sync(0xffffffffu, mbar_wait_cluster(&bar.p_full[slot], (j / kPSlots) & 1));
         if (!ok) break;
+        // the slot's next fill (tile j + kPSlots) cannot start before PV(j)
+        // frees it, and PV(j) waits for this warp's p_ok below
+        if (warp == 0 && lane == 0) mbar_arrive_expect_tx(&bar.p_full[slot], kPTx);
         ++pdone;
         const float m_new = *reinterpret_cast<const volatile float*>(smem + kOffP + slot * kPSlotBytes + kPBytes + 4 * h);
-        const bool need = m_new != m_prev && m_prev != -INFINITY;
+        // a tile computed with m = -inf has P = 0 and leaves O as it is
+        const bool need = m_new != m_prev && m_prev != -INFINITY && m_new != -INFINITY;
         if (__any_sync(0xffffffffu, need)) {
           // O holds PV(0..j-1): wait for PV(j-1), then scale this warp's rows.
           // PV(j - 1 - kPSlots) is complete (P(j) needed its slot), and PV(j)
@@ -653,7 +709,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(DecodeArgs a) {
           }
           tmem_wait_st();
         }
-        m_prev = m_new;
+        if (m_new != -INFINITY) m_prev = m_new;
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&bar.p_ok[slot]);
@@ -815,7 +871,11 @@ cudaError_t launch_unit_order(const DecodeArgs& a, int32_t units, int32_t* order
   return cudaGetLastError();
 }
 
-bool decode_tc_supported(const DecodeArgs& a) { return a.H <= 128 && (a.plan.chunk % kTile) == 0; }
+// (Cache rows are addressed in 31 bits: a cache of 2^31 rows would be 2.5 TB.)
+bool decode_tc_supported(const DecodeArgs& a) {
+  return a.H <= 128 && (a.plan.chunk % kTile) == 0 &&
+         static_cast<int64_t>(a.num_blocks) * a.block_size <= 0x7fffffffLL;
+}
 
 cudaError_t launch_decode_tc(const DecodeArgs& a, cudaStream_t st) {
   if (!decode_tc_supported(a)) return cudaErrorInvalidValue;
