@@ -368,26 +368,39 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(DecodeArgs a) {
     cp_async_wait<0>();
   } else if (score && warp == 10) {
     // ------------------------------------------------- score CTA forwarder
-    // Once this CTA's own rows of tile j have landed, make them visible to
-    // the async proxy (one proxy fence here serves the S issuers too, through
-    // kv_full); once the value CTA's receive slot is free, copy chunks 0-3
-    // (16 KB) into it.
+    // Two streams of tiles, each in order, served as their conditions come
+    // true (non-blocking polls), so that neither waits behind the other:
+    //   fence: once this CTA's own rows of tile jf have landed, fence them
+    //          into the async proxy and arrive on kv_full (for S);
+    //   copy:  once tile jc < jf is fenced and the value CTA's receive slot
+    //          is free, copy chunks 0-3 (16 KB) into it.
+    // (kv_loaded(jf + 5) needs S(jf), hence the fence of jf: no parity
+    // aliasing.)  The loop gives up after kWaitLimit polls without progress.
     bool ok = __all_sync(0xffffffffu, mbar_wait(&bar.q_ready, 0));
     // the value CTA's forwards into the stages (which held Q) may start
     if (ok && lane == 0) mbar_arrive_remote(map_peer(smem_u32(&bar.q_gone), peer));
-    for (int j = 0; j < ntiles && ok; ++j) {
-      const int st = j % kStages, rs = j % kRecv;
-      ok = __all_sync(0xffffffffu, mbar_wait(&bar.kv_loaded[st], (j / kStages) & 1));
-      if (!ok) break;
-      fence_proxy_async_smem();  // the producers' cp.async writes -> S and the bulk copy
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bar.kv_full[st]);
-      ok = __all_sync(0xffffffffu, mbar_wait_cluster(&bar.v_free[rs], ((j / kRecv) & 1) ^ 1));
-      if (!ok) break;
-      if (lane == 0)
-        bulk_copy_to_peer(map_peer(smem_base + kOffRecv + rs * kHalfBytes, peer), smem + kOffStages + st * kStageBytes,
-                          kHalfBytes, map_peer(smem_u32(&bar.v_full[rs]), peer));
-      __syncwarp();
+    int jf = 0, jc = 0;
+    uint32_t idle = 0;
+    while (ok && jc < ntiles) {
+      bool moved = false;
+      if (jf < ntiles && __all_sync(0xffffffffu, mbar_peek(&bar.kv_loaded[jf % kStages], (jf / kStages) & 1))) {
+        fence_proxy_async_smem();  // the producers' cp.async writes -> S and the bulk copy
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bar.kv_full[jf % kStages]);
+        ++jf;
+        moved = true;
+      }
+      if (jc < jf && __all_sync(0xffffffffu, mbar_peek_cluster(&bar.v_free[jc % kRecv], ((jc / kRecv) & 1) ^ 1))) {
+        const int st = jc % kStages, rs = jc % kRecv;
+        if (lane == 0)
+          bulk_copy_to_peer(map_peer(smem_base + kOffRecv + rs * kHalfBytes, peer),
+                            smem + kOffStages + st * kStageBytes, kHalfBytes, map_peer(smem_u32(&bar.v_full[rs]), peer));
+        __syncwarp();
+        ++jc;
+        moved = true;
+      }
+      idle = moved ? 0u : idle + 1u;
+      if (idle > kWaitLimit) ok = false;
     }
     if (!ok) set_abort(bar, a.dev_error);
   } else if (!score && warp == 8) {

@@ -96,6 +96,20 @@ __device__ __forceinline__ bool mbar_peek(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
+// Non-blocking probe with cluster-scope acquire (barriers completed by the
+// peer CTA).
+__device__ __forceinline__ bool mbar_peek_cluster(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 // Cluster-scope acquire variant (for barriers completed by the peer CTA).
 __device__ __forceinline__ bool mbar_test_cluster(uint64_t* bar, uint32_t parity) {
   uint32_t ok;
