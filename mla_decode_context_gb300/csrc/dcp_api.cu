@@ -14,7 +14,7 @@ namespace dcp {
 namespace {
 constexpr int kTargetCtasPerUnit = 2;  // CTAs the decode spends on one (row, shard, split)
 constexpr int32_t kMinSplitTokens = 256;
-constexpr int32_t kSplitRound = 64;
+constexpr int32_t kSplitRound = 32;  // split chunks in whole 32-token tiles
 constexpr int kMaxSplits = 32;
 
 // CTAs one wave of the decode can hold: the tensor-core kernel's resident
