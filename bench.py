@@ -377,6 +377,7 @@ def run_gb300(args, spec):
                        "parallelism": "replicas" if ws > 1 else "single",
                        "l2": "flushed before every step (512 MB write, untimed)"},
             "decode_ms": dec_avg, "combine_ms": com_avg,
+            "decode_ms_median": float(np.median(dec_ms)), "combine_ms_median": float(np.median(com_ms)),
             "decode_gbs": achieved, "combine_gbs": cbytes / (com_avg * 1e-3) / 1e9,
             "combine_hbm_frac": cbytes / (com_avg * 1e-3) / 1e9 / peak,
             "roofline": ({"bound": "tensor", "kernel": "dcp_mla_decode_partial", "achieved": tflops,
@@ -415,7 +416,7 @@ def run_gb300(args, spec):
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--workload", default=wl.LONG_120K.name, choices=sorted(wl.DECODE_WORKLOADS))

@@ -36,6 +36,10 @@ SMALL = [
     # under both parametrisations
     wl.DecodeSpec("h256_d4_i2_wide_heads", seed=41, B=2, seq_lens=(300, 1000), H=256, block_size=16, D=4,
                   interleave=2),
+    # one shard, long: 32 splits of 9 tiles, more than the split merge
+    # loads at once (its batched path)
+    wl.DecodeSpec("h128_d1_32_splits", seed=42, B=1, seq_lens=(9000,), H=128, block_size=64, D=1,
+                  interleave=1),
     # more units than clusters, so one split per shard: 20-25 tiles per unit
     # (every stage, S buffer and P slot reused several times)
     wl.DecodeSpec("h128_b12_unsplit", seed=39, B=12,
