@@ -43,8 +43,8 @@ KV_ROW_BYTES = 576 * 2
 MEASURED_TRAFFIC = {
     "workload": "long_ctx_120k_b1_d8_i1",
     "source": "mla_decode_context_gb300/csrc/dcp_decode_tc.cu",
-    "sha256": "9fb870fec144820aad95f44877d5579a28adeacf95273d5c2677939834cd20ba",
-    "bytes": 138482176 + 3941888,
+    "sha256": "087b48f9079aa297584983834872647c73c7b55ea0dbce2e4812179de1992fe6",
+    "bytes": 138481152 + 3569664,
 }
 
 

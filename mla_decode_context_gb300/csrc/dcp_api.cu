@@ -195,6 +195,8 @@ dcp_status_t dcp_mla_decode_partial(const void* q, int64_t q_stride_tok, const v
   a.scale = scale;
   a.plan = plan;
   a.dev_error = dev_error;
+  const char* stall = std::getenv("DCP_TEST_STALL_WAIT");  // failure-path test hook (see DecodeArgs)
+  a.stall_test = stall && stall[0] == '1';
   float* ws_O = nullptr;
   float* ws_lse = nullptr;
   if (plan.splits > 1) {

@@ -132,6 +132,7 @@ struct __align__(8) Bars {
   uint64_t fin[1 + kSParts * kSBuf];  // each issuing warp's MMAs complete
   uint64_t m_pub[8];          // score: running max after tile j posted (phase j / 8 of m_pub[j % 8]; 4 warps)
   uint64_t sm_fin;            // score: both softmax groups' final l and m written (8 warps)
+  uint64_t never;             // test hook only: initialised, never arrived on
   // score: valid rows of tile j in mask[j % 16] (written by the producer
   // before it arms kv_full; the slot is rewritten 16 tiles later, long after
   // the softmax of tile j has read it: a producer nine or more tiles ahead
@@ -228,6 +229,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(DecodeArgs a) {
     for (int i = 0; i < 1 + kSParts * kSBuf; ++i) mbar_init(&bar.fin[i], 1);
     for (int i = 0; i < 8; ++i) mbar_init(&bar.m_pub[i], 4);
     mbar_init(&bar.sm_fin, 8);
+    mbar_init(&bar.never, 1);
     bar.abort = 0;
     fence_mbar_init();
     if (!score) {
@@ -513,7 +515,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(DecodeArgs a) {
     const int sw = (h >> 1) & 3;  // 64-byte swizzle of row h
     const uint32_t p_row = static_cast<uint32_t>((h >> 3) * 512 + (h & 7) * 64);
     bool ok = true;
-    for (int j = sg; j < ntiles; j += 2) {
+    // failure-path test hook: a wait that runs out (nothing completes `never`)
+    if (a.stall_test && sg == 0) ok = __all_sync(0xffffffffu, mbar_wait(&bar.never, 0));
+    for (int j = sg; ok && j < ntiles; j += 2) {
       const int b = j % kSBuf, slot = j % kPSlots;
       // the other group's m after tile k, read early so that the load's
       // latency overlaps the wait for S.  Slot k % 8 is posted again at tile

@@ -31,6 +31,11 @@ struct DecodeArgs {
   // Optional launch order of the tensor-core decode's units (cluster c runs
   // unit unit_order[c]); nullptr = index order.
   const int32_t* unit_order;
+  // Test hook for the failure path (0 in normal use): nonzero makes the
+  // tensor-core decode's first softmax group wait on a barrier that nothing
+  // completes, so every unit ends through its bounded waits and reports
+  // DCP_DEVERR_TIMEOUT.
+  int32_t stall_test;
 };
 
 // Generic LSE merge over `nsrc` sources: pair p (flattened) reads

@@ -155,6 +155,26 @@ def test_bad_block_id_is_flagged_not_trapped(kernel):
     G.check_partials(O.cpu().numpy()[:, rows], lse.cpu().numpy()[:, rows], O_ref, lse_ref, "req1")
 
 
+def test_wait_that_runs_out_is_reported_and_the_context_survives(monkeypatch):
+    """Failure detection without a fault: a test hook makes one wait of the
+    tensor-core decode run out (a barrier nothing completes).  Every wait is
+    bounded, so the launch ends on its own, with DCP_DEVERR_TIMEOUT in
+    dev_error, and the next decode on the same context is correct."""
+    monkeypatch.delenv("DCP_FORCE_SIMT", raising=False)
+    spec = wl.DecodeSpec("stall_h128_d1", seed=43, B=1, seq_lens=(200,), H=128, block_size=64, D=1,
+                         interleave=1)
+    inp = wl.make_decode_inputs(spec)
+    t = G.to_device(inp)
+    monkeypatch.setenv("DCP_TEST_STALL_WAIT", "1")
+    _, _, err = G.run_decode(inp, t)
+    assert err & dcp.DEVERR_TIMEOUT
+    monkeypatch.delenv("DCP_TEST_STALL_WAIT")
+    O, lse, err = G.run_decode(inp, t)
+    assert err == 0
+    O_ref, lse_ref, rows = oracle.decode_partial(inp)
+    G.check_partials(O.cpu().numpy()[:, rows], lse.cpu().numpy()[:, rows], O_ref, lse_ref, spec.name)
+
+
 def test_seq_len_above_declared_max_is_flagged():
     inp = wl.make_decode_inputs(SMALL[7])
     t = G.to_device(inp)
