@@ -43,6 +43,16 @@
  *     DCP_KV_DIM = 576 bf16 values (512 compressed-KV dims followed by 64
  *     rope dims); values are the first DCP_LATENT_DIM = 512 dims.
  *   - LSEs are natural logarithms; -inf marks "no tokens".
+ *   - Two environment variables, read on every call and unset in normal use,
+ *     change what dcp_mla_decode_partial runs:
+ *       DCP_FORCE_SIMT=1       the CUDA-core reference kernel instead of the
+ *                              tensor-core one (A/B checks);
+ *       DCP_TEST_STALL_WAIT=1  test hook for the failure path: one wait of
+ *                              the tensor-core kernel runs out on purpose
+ *                              (on a barrier nothing completes), so the call
+ *                              ends with DCP_DEVERR_TIMEOUT in *dev_error
+ *                              after about a second per bounded wait; the
+ *                              outputs are undefined.
  */
 #ifndef DCP_H_
 #define DCP_H_

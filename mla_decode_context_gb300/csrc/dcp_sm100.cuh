@@ -1,5 +1,5 @@
 // Thin inline-PTX wrappers for the Blackwell (sm_100 family, here sm_103a)
-// features the tensor-core decode uses: mbarriers, TMA tensor loads, bulk
+// features the tensor-core decode uses: mbarriers, cp.async, bulk
 // shared-memory copies between the two CTAs of a cluster, and tcgen05
 // (TMEM allocation, MMA, commit, TMEM loads/stores).  Every wait is bounded:
 // it gives up after a fixed number of polls and reports failure, so a
@@ -142,54 +142,15 @@ __device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity
 // ---------------------------------------------------------------------------
 // proxies
 // ---------------------------------------------------------------------------
-// Generic-proxy shared-memory writes -> visible to the async proxy (TMA,
-// bulk copies, tensor-core operand reads).
+// Generic-proxy shared-memory writes (cp.async, st.shared) -> visible to the
+// async proxy (bulk copies, tensor-core operand reads).
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
-// Named barrier among `nthreads` threads (id 1..15; 0 is __syncthreads).
-__device__ __forceinline__ void named_bar(uint32_t id, uint32_t nthreads) {
-  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
-}
-
 // ---------------------------------------------------------------------------
-// TMA (tiled tensor loads) and bulk copies
+// bulk copies and asynchronous stores between the CTAs of a cluster; cp.async
 // ---------------------------------------------------------------------------
-__device__ __forceinline__ void tma_prefetch_desc(const void* tmap) {
-  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tmap)) : "memory");
-}
-
-__device__ __forceinline__ void tma_load_2d(void* dst, const void* tmap, uint64_t* bar, int32_t c0, int32_t c1) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%3, %4}], [%2];" ::"r"(smem_u32(dst)),
-      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(smem_u32(bar)), "r"(c0), "r"(c1)
-      : "memory");
-}
-
-__device__ __forceinline__ void tma_load_5d(void* dst, const void* tmap, uint64_t* bar, int32_t c0, int32_t c1,
-                                            int32_t c2, int32_t c3, int32_t c4) {
-  asm volatile(
-      "cp.async.bulk.tensor.5d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%3, %4, %5, %6, %7}], [%2];" ::"r"(smem_u32(dst)),
-      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4)
-      : "memory");
-}
-
-// Multicast form of tma_load_5d: the box lands at the same shared-memory
-// offset in every CTA of the cluster named in `cta_mask`, and each of them
-// gets the tx bytes on its mbarrier at the offset of `bar`.
-__device__ __forceinline__ void tma_load_5d_mc(void* dst, const void* tmap, uint64_t* bar, int32_t c0, int32_t c1,
-                                               int32_t c2, int32_t c3, int32_t c4, uint16_t cta_mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.5d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster"
-      " [%0], [%1, {%3, %4, %5, %6, %7}], [%2], %8;" ::"r"(smem_u32(dst)),
-      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4),
-      "h"(cta_mask)
-      : "memory");
-}
-
 // Copy `bytes` (multiple of 16) from this CTA's shared memory to the peer's
 // (`dst_peer`, `bar_peer` from map_peer); completes tx bytes on the peer's
 // mbarrier.
@@ -202,16 +163,6 @@ __device__ __forceinline__ void bulk_copy_to_peer(uint32_t dst_peer, const void*
       : "memory");
 }
 
-// 16-byte store into the peer CTA's shared memory (`dst_peer` from
-// map_peer) that completes 16 tx bytes on the peer's mbarrier `bar_peer`.
-__device__ __forceinline__ void st_async_peer(uint32_t dst_peer, float4 v, uint32_t bar_peer) {
-  asm volatile(
-      "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(dst_peer),
-      "r"(__float_as_uint(v.x)), "r"(__float_as_uint(v.y)), "r"(__float_as_uint(v.z)), "r"(__float_as_uint(v.w)),
-      "r"(bar_peer)
-      : "memory");
-}
-
 // 4-byte store into the peer CTA's shared memory that completes 4 tx bytes
 // on the peer's mbarrier `bar_peer`.
 __device__ __forceinline__ void st_async_peer_b32(uint32_t dst_peer, uint32_t v, uint32_t bar_peer) {
@@ -220,12 +171,9 @@ __device__ __forceinline__ void st_async_peer_b32(uint32_t dst_peer, uint32_t v,
                : "memory");
 }
 
-// 16-byte global -> shared copy through L2 (LSU path, bypasses L1).
-__device__ __forceinline__ void cp_async16(uint32_t dst_smem, const void* src) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst_smem), "l"(src) : "memory");
-}
-// Same, with a source size of 0 or 16 bytes: 0 writes 16 zero bytes and
-// reads nothing (for rows that must not be loaded).
+// 16-byte global -> shared copy through L2 (LSU path, bypasses L1) with a
+// source size of 0 or 16 bytes: 0 writes 16 zero bytes and reads nothing
+// (for rows that must not be loaded).
 __device__ __forceinline__ void cp_async16_zfill(uint32_t dst_smem, const void* src, uint32_t src_bytes) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst_smem), "l"(src), "r"(src_bytes) : "memory");
 }
@@ -314,15 +262,6 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
         "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]),
         "=r"(r[30]), "=r"(r[31])
       : "r"(taddr)
-      : "memory");
-}
-
-__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
-  asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, "
-      "%14, %15, %16};" ::"r"(taddr),
-      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
-      "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
       : "memory");
 }
 
