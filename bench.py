@@ -413,6 +413,25 @@ def run_gb300(args, spec):
     return 0
 
 
+def run_decode_only(args, spec):
+    """For profilers: warmup + steps calls of the decode on one GPU, nothing
+    timed or printed but a one-line summary; exits nonzero on a device error."""
+    import torch
+    import mla_decode_context_gb300 as dcp
+    inp = wl.make_decode_inputs(spec)
+    t = wl.to_torch(inp, "cuda:0")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda:0")
+    for _ in range(args.warmup + args.steps):
+        dcp.decode_partial(t["q"], t["kv_cache"], t["block_table"], t["seq_lens"], t["query_start_loc"],
+                           D=inp["D"], interleave=inp["interleave"], scale=inp["scale"],
+                           max_seq_len=inp["max_seq_len"], max_q_len=inp["max_q_len"], dev_error=err)
+    torch.cuda.synchronize()
+    flags = int(err.item())
+    print("%s: %d decode calls, dev_error 0x%x, KV bytes %d"
+          % (spec.name, args.warmup + args.steps, flags, kv_tokens(inp) * KV_ROW_BYTES), flush=True)
+    return 1 if flags else 0
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -420,8 +439,12 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--workload", default=wl.LONG_120K.name, choices=sorted(wl.DECODE_WORKLOADS))
+    ap.add_argument("--decode-only", action="store_true",
+                    help="only call the decode warmup + steps times (for ncu captures)")
     args = ap.parse_args(argv)
     spec = wl.DECODE_WORKLOADS[args.workload]
+    if args.decode_only:
+        return run_decode_only(args, spec)
     if args.impl == "reference":
         return run_reference(args, spec)
     return run_gb300(args, spec)
