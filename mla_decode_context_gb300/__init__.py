@@ -99,6 +99,19 @@ def _stream(stream) -> ctypes.c_void_p:
     return ctypes.c_void_p(int(stream))
 
 
+def _need_opt(t: Optional[torch.Tensor], name: str, dtype=None, allow_empty=False):
+    """Optional device buffers (workspace, dev_error): the kernels write them,
+    so a host tensor here would be a host address on the device."""
+    if t is None:
+        return
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise ValueError("%s must be a CUDA tensor or None" % name)
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError("%s must be %s, got %s" % (name, dtype, t.dtype))
+    if t.numel() == 0 and not allow_empty:
+        raise ValueError("%s must not be empty" % name)
+
+
 def _check(st: int, where: str):
     if st != 0:
         raise DCPError(st, where)
@@ -176,6 +189,10 @@ def dcp_mla_decode_partial(q, kv_cache, block_table, seq_lens, query_start_loc, 
         raise ValueError("seq_lens, query_start_loc and block_table disagree on B")
     if tuple(O_part.shape) != (D, T, H, LATENT_DIM) or tuple(lse_part.shape) != (D, T, H):
         raise ValueError("O_part must be [D, T, H, 512] and lse_part [D, T, H]")
+    _need_opt(workspace, "workspace", allow_empty=True)
+    if workspace is not None and workspace.numel() == 0:
+        workspace = None
+    _need_opt(dev_error, "dev_error", torch.int32)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     st = lib().dcp_mla_decode_partial(
         _ptr(q), q.stride(0), _ptr(kv_cache), kv_cache.shape[0], kv_cache.shape[1], _ptr(block_table),
@@ -208,6 +225,7 @@ def dcp_mla_decode_partial_noalloc(q, kv_cache, block_table, seq_lens, query_sta
     B = seq_lens.shape[0]
     if tuple(O_part.shape) != (D, T, H, LATENT_DIM) or tuple(lse_part.shape) != (D, T, H):
         raise ValueError("O_part must be [D, T, H, 512] and lse_part [D, T, H]")
+    _need_opt(dev_error, "dev_error", torch.int32)
     st = lib().dcp_mla_decode_partial_noalloc(
         _ptr(q), q.stride(0), _ptr(kv_cache), kv_cache.shape[0], kv_cache.shape[1], _ptr(block_table),
         block_table.shape[1], block_table.stride(0), _ptr(seq_lens), _ptr(query_start_loc), B, T, H,
