@@ -112,6 +112,38 @@ def _need_opt(t: Optional[torch.Tensor], name: str, dtype=None, allow_empty=Fals
         raise ValueError("%s must not be empty" % name)
 
 
+try:  # NVTX ranges name the library calls on profiler timelines
+    from torch.cuda import nvtx as _nvtx
+except Exception:  # pragma: no cover
+    _nvtx = None
+
+
+class _Range:
+    """NVTX range around one library call; a no-op where NVTX is missing
+    (it never raises)."""
+
+    def __init__(self, name: str):
+        self.name = name
+        self.pushed = False
+
+    def __enter__(self):
+        if _nvtx is not None:
+            try:
+                _nvtx.range_push(self.name)
+                self.pushed = True
+            except Exception:
+                pass
+        return self
+
+    def __exit__(self, *exc):
+        if self.pushed:
+            try:
+                _nvtx.range_pop()
+            except Exception:
+                pass
+        return False
+
+
 def _check(st: int, where: str):
     if st != 0:
         raise DCPError(st, where)
@@ -194,11 +226,12 @@ def dcp_mla_decode_partial(q, kv_cache, block_table, seq_lens, query_start_loc, 
         workspace = None
     _need_opt(dev_error, "dev_error", torch.int32)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
-    st = lib().dcp_mla_decode_partial(
-        _ptr(q), q.stride(0), _ptr(kv_cache), kv_cache.shape[0], kv_cache.shape[1], _ptr(block_table),
-        block_table.shape[1], block_table.stride(0), _ptr(seq_lens), _ptr(query_start_loc), B, T, H,
-        max_seq_len, max_q_len, D, interleave, scale, _ptr(O_part), _ptr(lse_part), _ptr(workspace),
-        ws_bytes, _ptr(dev_error), _stream(stream))
+    with _Range("dcp_mla_decode_partial"):
+        st = lib().dcp_mla_decode_partial(
+            _ptr(q), q.stride(0), _ptr(kv_cache), kv_cache.shape[0], kv_cache.shape[1], _ptr(block_table),
+            block_table.shape[1], block_table.stride(0), _ptr(seq_lens), _ptr(query_start_loc), B, T, H,
+            max_seq_len, max_q_len, D, interleave, scale, _ptr(O_part), _ptr(lse_part), _ptr(workspace),
+            ws_bytes, _ptr(dev_error), _stream(stream))
     _check(st, "dcp_mla_decode_partial")
 
 
@@ -226,11 +259,12 @@ def dcp_mla_decode_partial_noalloc(q, kv_cache, block_table, seq_lens, query_sta
     if tuple(O_part.shape) != (D, T, H, LATENT_DIM) or tuple(lse_part.shape) != (D, T, H):
         raise ValueError("O_part must be [D, T, H, 512] and lse_part [D, T, H]")
     _need_opt(dev_error, "dev_error", torch.int32)
-    st = lib().dcp_mla_decode_partial_noalloc(
-        _ptr(q), q.stride(0), _ptr(kv_cache), kv_cache.shape[0], kv_cache.shape[1], _ptr(block_table),
-        block_table.shape[1], block_table.stride(0), _ptr(seq_lens), _ptr(query_start_loc), B, T, H,
-        max_seq_len, max_q_len, D, interleave, scale, _ptr(O_part), _ptr(lse_part), _ptr(dev_error),
-        _stream(stream))
+    with _Range("dcp_mla_decode_partial_noalloc"):
+        st = lib().dcp_mla_decode_partial_noalloc(
+            _ptr(q), q.stride(0), _ptr(kv_cache), kv_cache.shape[0], kv_cache.shape[1], _ptr(block_table),
+            block_table.shape[1], block_table.stride(0), _ptr(seq_lens), _ptr(query_start_loc), B, T, H,
+            max_seq_len, max_q_len, D, interleave, scale, _ptr(O_part), _ptr(lse_part), _ptr(dev_error),
+            _stream(stream))
     _check(st, "dcp_mla_decode_partial_noalloc")
 
 
@@ -255,8 +289,9 @@ def dcp_lse_combine(O_part, lse_part, seq_lens, query_start_loc, out, out_lse, *
     if not (out_lse.is_contiguous() or out_lse.data_ptr() == lse_part.data_ptr()):
         raise ValueError("out_lse must be contiguous")
     B = seq_lens.shape[0]
-    st = lib().dcp_lse_combine(_ptr(O_part), _ptr(lse_part), _ptr(seq_lens), _ptr(query_start_loc), B, T, H,
-                               D, _ptr(out), dt, _ptr(out_lse), _stream(stream))
+    with _Range("dcp_lse_combine"):
+        st = lib().dcp_lse_combine(_ptr(O_part), _ptr(lse_part), _ptr(seq_lens), _ptr(query_start_loc), B, T,
+                                   H, D, _ptr(out), dt, _ptr(out_lse), _stream(stream))
     _check(st, "dcp_lse_combine")
 
 
