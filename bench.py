@@ -216,6 +216,14 @@ def barrier():
         dist.barrier()
 
 
+def workload_config(spec, inp, n_gpus: int) -> dict:
+    """The `config` object of a bench line, the same for both arms."""
+    return {"workload": spec.name, "B": spec.B, "seq_len": int(inp["max_seq_len"]), "H": spec.H,
+            "D": spec.D, "interleave": spec.interleave, "block_size": spec.block_size,
+            "q_len": int(inp["max_q_len"]), "parallelism": "replicas" if n_gpus > 1 else "single",
+            "l2": "flushed before every timed step (512 MB write, untimed)"}
+
+
 def run_reference(args, spec):
     ws, rank, _ = dist_env()
     if rank != 0:
@@ -239,16 +247,194 @@ def run_reference(args, spec):
         "impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * el / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic",
-        "config": {"workload": spec.name, "B": spec.B, "seq_len": int(inp["max_seq_len"]), "H": spec.H,
-                   "D": spec.D, "interleave": spec.interleave, "block_size": spec.block_size},
+        "data": "synthetic", "config": workload_config(spec, inp, args.gpus),
         "cpu_baseline": {"value": v, "unit": UNIT, "cores": cores(), "kind": "oracle",
                          "sample": "the whole workload per step (decode partials for all 8 shards "
-                                   "+ combine, float64 numpy; BLAS threads = all host cores)"},
+                                   "+ combine, float64 numpy; BLAS threads = all host cores; host "
+                                   "caches are not flushed)"},
         "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
     return 0
+
+
+def capture(fn, use_graphs: bool):
+    """A CUDA graph of `fn` (library calls on the current stream), or None
+    when graphs are off or the capture fails (the caller then runs fn
+    eagerly).  Graph replay launches the same kernels without the host's
+    per-call launch gaps, as a serving loop replays its decode step."""
+    import torch
+    if not use_graphs:
+        return None
+    try:
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            fn()
+        torch.cuda.current_stream().wait_stream(s)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, capture_error_mode="thread_local"):
+            fn()
+        torch.cuda.synchronize()
+        return g
+    except Exception as e:  # pragma: no cover - depends on the driver
+        print("bench: graph capture failed (%s); timing eager calls" % e, file=sys.stderr)
+        torch.cuda.synchronize()
+        return None
+
+
+class DecodeBench:
+    """One decode workload resident on the device, with its outputs,
+    workspace and the two library calls of a step (decode, combine)."""
+
+    def __init__(self, spec, dev, use_graphs=True):
+        import torch
+        import mla_decode_context_gb300 as dcp
+        self.spec, self.dev = spec, dev
+        self.inp = inp = wl.make_decode_inputs(spec)
+        self.t = t = wl.to_torch(inp, dev)
+        D, T, H, I, B = inp["D"], inp["T"], inp["H"], inp["interleave"], inp["B"]
+        self.msl, self.mql = msl, mql = max(1, inp["max_seq_len"]), max(1, inp["max_q_len"])
+        self.O = O = torch.empty((D, T, H, 512), dtype=torch.float32, device=dev)
+        self.lse = lse = torch.empty((D, T, H), dtype=torch.float32, device=dev)
+        self.out = out = torch.empty((T, H, 512), dtype=torch.bfloat16, device=dev)
+        self.out_lse = out_lse = torch.empty((T, H), dtype=torch.float32, device=dev)
+        wsz = dcp.dcp_decode_workspace_size(B, T, H, D, msl, mql)
+        self.work = work = torch.empty(max(wsz, 16), dtype=torch.uint8, device=dev) if wsz else None
+        self.derr = derr = torch.zeros(1, dtype=torch.int32, device=dev)
+        self.launches = 1 + dcp.dcp_decode_kernel_launches(B, T, H, D, I, msl, mql,
+                                                           work.numel() if work is not None else 0)
+
+        def decode():
+            dcp.dcp_mla_decode_partial(t["q"], t["kv_cache"], t["block_table"], t["seq_lens"],
+                                       t["query_start_loc"], O, lse, D=D, interleave=I, scale=inp["scale"],
+                                       max_seq_len=msl, max_q_len=mql, workspace=work, dev_error=derr)
+
+        def combine():
+            dcp.dcp_lse_combine(O, lse, t["seq_lens"], t["query_start_loc"], out, out_lse)
+
+        self.decode, self.combine = decode, combine
+        for _ in range(3):
+            decode()
+            combine()
+        torch.cuda.synchronize()
+        self.check_flags("warm-up")
+        self.g_dec = capture(decode, use_graphs)
+        self.g_com = capture(combine, use_graphs)
+        self.graphs = self.g_dec is not None and self.g_com is not None
+
+    def check_flags(self, where):
+        # a kernel that reported a bad input or a timed-out wait did not do
+        # the work being timed: stop instead of printing a number
+        flags = int(self.derr.item())
+        if flags:
+            raise SystemExit(f"bench: device error flags 0x{flags:x} after {where} ({self.spec.name})")
+
+    def run_decode(self):
+        self.g_dec.replay() if self.graphs else self.decode()
+
+    def run_combine(self):
+        self.g_com.replay() if self.graphs else self.combine()
+
+    def timed(self, steps, warmup, flush):
+        """Per-step (decode ms, combine ms), CUDA events on the launching
+        stream, the L2 flushed (untimed) before every step."""
+        import torch
+        stream = torch.cuda.current_stream(self.dev)
+        for _ in range(warmup):
+            flush.zero_()
+            self.run_decode()
+            self.run_combine()
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
+        torch.cuda.synchronize()
+        for k in range(steps):
+            flush.zero_()
+            ev[k][0].record(stream)
+            self.run_decode()
+            ev[k][1].record(stream)
+            self.run_combine()
+            ev[k][2].record(stream)
+        torch.cuda.synchronize()
+        self.check_flags("the timed steps")
+        dec = [ev[k][0].elapsed_time(ev[k][1]) for k in range(steps)]
+        com = [ev[k][1].elapsed_time(ev[k][2]) for k in range(steps)]
+        return dec, com
+
+    def roofline(self, dec_ms: float, traffic=None) -> dict:
+        """The decode call's roofline record: HBM unless the workload's flop
+        per byte pass the measured ridge (verification rows)."""
+        inp = self.inp
+        peak, peak_kind = peaks()
+        tpeak, tpeak_kind = tensor_peak()
+        dbytes = decode_bytes(inp)
+        dflops = decode_flops(inp)
+        achieved = dbytes / (dec_ms * 1e-3) / 1e9
+        tflops = dflops / (dec_ms * 1e-3) / 1e12
+        if dflops / dbytes > tpeak * 1e12 / (peak * 1e9):
+            return {"bound": "tensor", "kernel": "dcp_mla_decode_partial", "achieved": tflops, "peak": tpeak,
+                    "unit": "TFLOP/s", "frac": tflops / tpeak,
+                    "peak_source": tpeak_kind + " (MEASURED_PEAKS.json bf16_tflops, burst)"
+                    if tpeak_kind == "measured" else "fallback 1.9 PFLOP/s",
+                    "hbm_achieved_gbs": achieved, "hbm_frac": achieved / peak, "traffic": traffic,
+                    "algorithmic_flops_per_launch": dflops, "algorithmic_bytes_per_launch": dbytes}
+        return {"bound": "hbm", "kernel": "dcp_mla_decode_partial", "achieved": achieved, "peak": peak,
+                "unit": "GB/s", "frac": achieved / peak,
+                "peak_source": peak_kind + " (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
+                else "fallback 6.8 TB/s", "traffic": traffic,
+                "tensor_achieved_tflops": tflops, "tensor_frac": tflops / tpeak,
+                "algorithmic_bytes_per_launch": dbytes}
+
+    def release(self):
+        import torch
+        for k in list(vars(self)):
+            setattr(self, k, None)
+        torch.cuda.empty_cache()
+
+
+def combine_sweep_record(dev, flush, steps: int = 20):
+    """The standalone combine over the sweep (D in {2, 4, 8}, T in {1, 64,
+    1024, 4096}, H = 128): median µs per call and GB/s of algorithmic bytes
+    (live partials + all LSEs read, bf16 out + fp32 out_lse written); the HBM
+    fraction is reported where the pages' bandwidth target applies (T >=
+    1024; smaller T are latency-bound)."""
+    import torch
+    import mla_decode_context_gb300 as dcp
+    peak, _ = peaks()
+    rec = {}
+    for D, T in wl.COMBINE_SWEEP:
+        O, lse, seq, qsl, empty, pad = wl.make_combine_inputs(D, T, device=dev)
+        seq_t, qsl_t = torch.from_numpy(seq).to(dev), torch.from_numpy(qsl).to(dev)
+        out = torch.empty((T, wl.COMBINE_H, 512), dtype=torch.bfloat16, device=dev)
+        out_lse = torch.empty((T, wl.COMBINE_H), dtype=torch.float32, device=dev)
+
+        def call():
+            dcp.dcp_lse_combine(O, lse, seq_t, qsl_t, out, out_lse)
+
+        g = capture(call, True)
+        run = g.replay if g is not None else call
+        for _ in range(3):
+            run()
+        stream = torch.cuda.current_stream(dev)
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(steps)]
+        torch.cuda.synchronize()
+        for k in range(steps):
+            flush.zero_()
+            ev[k][0].record(stream)
+            run()
+            ev[k][1].record(stream)
+        torch.cuda.synchronize()
+        us = statistics.median(ev[k][0].elapsed_time(ev[k][1]) * 1e3 for k in range(steps))
+        live = (~empty & ~pad[None, :]).sum() * wl.COMBINE_H
+        nbytes = int(live) * 512 * 4 + D * T * wl.COMBINE_H * 4 + T * wl.COMBINE_H * (512 * 2 + 4)
+        gbs = nbytes / (us * 1e-6) / 1e9
+        r = {"us": us, "gbs": gbs, "algorithmic_bytes": nbytes}
+        if T >= 1024:
+            r["hbm_frac"] = gbs / peak
+        rec["D%d_T%d" % (D, T)] = r
+        del O, lse, out, out_lse, g
+        torch.cuda.empty_cache()
+    return rec
 
 
 def run_gb300(args, spec):
@@ -262,64 +448,20 @@ def run_gb300(args, spec):
     torch.cuda.set_device(dev)
     import mla_decode_context_gb300 as dcp
 
-    inp = wl.make_decode_inputs(spec)
-    t = wl.to_torch(inp, dev)
-    D, T, H, I = inp["D"], inp["T"], inp["H"], inp["interleave"]
-    B = inp["B"]
-    msl, mql = max(1, inp["max_seq_len"]), max(1, inp["max_q_len"])
-    O = torch.empty((D, T, H, 512), dtype=torch.float32, device=dev)
-    lse = torch.empty((D, T, H), dtype=torch.float32, device=dev)
-    out = torch.empty((T, H, 512), dtype=torch.bfloat16, device=dev)
-    out_lse = torch.empty((T, H), dtype=torch.float32, device=dev)
-    wsz = dcp.dcp_decode_workspace_size(B, T, H, D, msl, mql)
-    work = torch.empty(max(wsz, 16), dtype=torch.uint8, device=dev) if wsz else None
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
-    derr = torch.zeros(1, dtype=torch.int32, device=dev)
-    stream = torch.cuda.current_stream(dev)
-
-    def check_device_flags(where):
-        # a kernel that reported a bad input or a timed-out wait did not do
-        # the work being timed: stop instead of printing a number
-        flags = int(derr.item())
-        if flags:
-            raise SystemExit(f"bench: device error flags 0x{flags:x} after {where}")
-
-    def decode():
-        dcp.dcp_mla_decode_partial(t["q"], t["kv_cache"], t["block_table"], t["seq_lens"],
-                                   t["query_start_loc"], O, lse, D=D, interleave=I, scale=inp["scale"],
-                                   max_seq_len=msl, max_q_len=mql, workspace=work, dev_error=derr,
-                                   stream=stream)
-
-    def combine():
-        dcp.dcp_lse_combine(O, lse, t["seq_lens"], t["query_start_loc"], out, out_lse, stream=stream)
-
-    for _ in range(max(3, args.warmup)):
-        decode()
-        combine()
-    torch.cuda.synchronize()
-    check_device_flags("warm-up")
-    launches_per_step = 1 + dcp.dcp_decode_kernel_launches(B, T, H, D, I, msl, mql, work.numel() if work is not None else 0)
+    bench = DecodeBench(spec, dev, use_graphs=not args.eager)
+    inp, t = bench.inp, bench.t
 
     # ---- device-timed steps (inputs resident, L2 flushed before each) ----
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
     barrier()
     torch.cuda.synchronize()
     clocks = Clocks(dev.index) if rank == 0 else None
     time.sleep(0.3 if clocks else 0)
     wall0 = time.perf_counter()
-    for k in range(args.steps):
-        flush.zero_()
-        ev[k][0].record(stream)
-        decode()
-        ev[k][1].record(stream)
-        combine()
-        ev[k][2].record(stream)
-    torch.cuda.synchronize()
+    dec_ms, com_ms = bench.timed(args.steps, max(3, args.warmup), flush)
     wall = time.perf_counter() - wall0
     barrier()
     ck = clocks.stop() if clocks else None
-    dec_ms = [ev[k][0].elapsed_time(ev[k][1]) for k in range(args.steps)]
-    com_ms = [ev[k][1].elapsed_time(ev[k][2]) for k in range(args.steps)]
     step_ms = sum(a + b for a, b in zip(dec_ms, com_ms)) / args.steps
     step_ms = max_over_ranks(step_ms, dev)
     dec_avg = sum(dec_ms) / len(dec_ms)
@@ -331,8 +473,8 @@ def run_gb300(args, spec):
     htab = t["block_table"].cpu().pin_memory()
     hseq = t["seq_lens"].cpu().pin_memory()
     hqsl = t["query_start_loc"].cpu().pin_memory()
-    hout = torch.empty_like(out, device="cpu").pin_memory()
-    hlse = torch.empty_like(out_lse, device="cpu").pin_memory()
+    hout = torch.empty_like(bench.out, device="cpu").pin_memory()
+    hlse = torch.empty_like(bench.out_lse, device="cpu").pin_memory()
     h2d = sum(x.numel() * x.element_size() for x in (hq, htab, hseq, hqsl))
     d2h = hout.numel() * hout.element_size() + hlse.numel() * hlse.element_size()
     e2e_ms = []
@@ -344,67 +486,65 @@ def run_gb300(args, spec):
         t["block_table"].copy_(htab, non_blocking=True)
         t["seq_lens"].copy_(hseq, non_blocking=True)
         t["query_start_loc"].copy_(hqsl, non_blocking=True)
-        decode()
-        combine()
-        hout.copy_(out, non_blocking=True)
-        hlse.copy_(out_lse, non_blocking=True)
+        bench.decode()
+        bench.combine()
+        hout.copy_(bench.out, non_blocking=True)
+        hlse.copy_(bench.out_lse, non_blocking=True)
         torch.cuda.synchronize()
         e2e_ms.append(1e3 * (time.perf_counter() - w0))
     e2e_avg = max_over_ranks(sum(e2e_ms) / len(e2e_ms), dev)
-    check_device_flags("the timed steps")
+    bench.check_flags("the end-to-end steps")
 
     tokens = kv_tokens(inp)
-    peak, peak_kind = peaks()
-    dbytes = decode_bytes(inp)
-    achieved = dbytes / (dec_avg * 1e-3) / 1e9
-    # the bound is the roof the workload meets first: HBM unless its flop
-    # per byte exceeds the measured ridge (verification rows, q_len > 1)
-    tpeak, tpeak_kind = tensor_peak()
-    dflops = decode_flops(inp)
-    tflops = dflops / (dec_avg * 1e-3) / 1e12
-    tensor_bound = dflops / dbytes > tpeak * 1e12 / (peak * 1e9)
-    cbytes = combine_bytes(inp, lse.cpu().numpy())
+    peak, _ = peaks()
+    cbytes = combine_bytes(inp, bench.lse.cpu().numpy())
+    roof = bench.roofline(dec_avg, measured_traffic(spec.name))
     res = None
     if rank == 0:
-        rate, passes, secs = cpu_oracle_rate(inp)
         res = {
             "metric": METRIC, "value": aggregate_rate(ws, tokens, step_ms), "unit": UNIT, "n_gpus": ws,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_ms,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": dcp.compute_dtype(), "data": "synthetic",
-            "config": {"workload": spec.name, "B": B, "seq_len": int(inp["max_seq_len"]), "H": H, "D": D,
-                       "interleave": I, "block_size": inp["block_size"], "q_len": mql,
-                       "parallelism": "replicas" if ws > 1 else "single",
-                       "l2": "flushed before every step (512 MB write, untimed)"},
+            "config": workload_config(spec, inp, ws),
+            "timing": "CUDA graphs of the library calls, replayed" if bench.graphs else "eager library calls",
             "decode_ms": dec_avg, "combine_ms": com_avg,
             "decode_ms_median": float(np.median(dec_ms)), "combine_ms_median": float(np.median(com_ms)),
-            "decode_gbs": achieved, "combine_gbs": cbytes / (com_avg * 1e-3) / 1e9,
+            "decode_gbs": decode_bytes(inp) / (dec_avg * 1e-3) / 1e9,
+            "combine_gbs": cbytes / (com_avg * 1e-3) / 1e9,
             "combine_hbm_frac": cbytes / (com_avg * 1e-3) / 1e9 / peak,
-            "roofline": ({"bound": "tensor", "kernel": "dcp_mla_decode_partial", "achieved": tflops,
-                          "peak": tpeak, "unit": "TFLOP/s", "frac": tflops / tpeak,
-                          "peak_source": tpeak_kind + " (MEASURED_PEAKS.json bf16_tflops, burst)"
-                          if tpeak_kind == "measured" else "fallback 1.9 PFLOP/s",
-                          "hbm_achieved_gbs": achieved, "hbm_frac": achieved / peak,
-                          "traffic": measured_traffic(spec.name),
-                          "algorithmic_flops_per_launch": dflops, "algorithmic_bytes_per_launch": dbytes}
-                         if tensor_bound else
-                         {"bound": "hbm", "kernel": "dcp_mla_decode_partial", "achieved": achieved,
-                          "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                          "peak_source": peak_kind + " (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
-                          else "fallback 6.8 TB/s", "traffic": measured_traffic(spec.name),
-                          "tensor_achieved_tflops": tflops, "tensor_frac": tflops / tpeak,
-                          "algorithmic_bytes_per_launch": dbytes}),
+            "roofline": roof,
             "e2e": {"value": aggregate_rate(ws, tokens, e2e_avg), "unit": UNIT, "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "note": "host-pinned per-step inputs (q, block table, "
                     "seq_lens, query_start_loc) copied in and out/out_lse copied back inside the timed "
-                    "region; the paged KV cache is resident device state"},
-            "gpu_launches": launches_per_step * args.steps,
+                    "region, library called eagerly; the paged KV cache is resident device state"},
+            "gpu_launches": bench.launches * args.steps,
             "clocks": ck,
             "wall_s_timed": wall,
-            "cpu_baseline": {"value": rate, "unit": UNIT, "cores": cores(), "kind": "oracle",
-                             "sample": "whole workload x %d passes (%.1f s): float64 numpy decode "
-                                       "partials + combine" % (passes, secs)},
         }
+    bench.release()
+
+    # ---- the other workloads: decode records and the combine sweep ----
+    if rank == 0 and not args.headline_only:
+        recs = {}
+        for other in (wl.BATCHED_B64, wl.SPEC_VERIFY_B32):
+            ob = DecodeBench(other, dev, use_graphs=not args.eager)
+            osteps = max(5, min(args.steps, 20))
+            d_ms, c_ms = ob.timed(osteps, 3, flush)
+            dmed = float(np.median(d_ms))
+            recs[other.name] = {
+                "config": workload_config(other, ob.inp, 1), "steps": osteps,
+                "decode_ms_median": dmed, "combine_ms_median": float(np.median(c_ms)),
+                "kv_tokens_per_s": kv_tokens(ob.inp) / ((dmed + float(np.median(c_ms))) * 1e-3),
+                "roofline": ob.roofline(dmed), "gpu_launches_per_step": ob.launches}
+            ob.release()
+        recs["combine_sweep_h128"] = combine_sweep_record(dev, flush)
+        res["workloads"] = recs
+    if rank == 0:
+        rate, passes, secs = cpu_oracle_rate(inp)
+        res["cpu_baseline"] = {"value": rate, "unit": UNIT, "cores": cores(), "kind": "oracle",
+                               "sample": "whole workload x %d passes (%.1f s): float64 numpy decode "
+                                         "partials + combine" % (passes, secs)}
     if ws > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
@@ -441,6 +581,9 @@ def main(argv=None):
     ap.add_argument("--workload", default=wl.LONG_120K.name, choices=sorted(wl.DECODE_WORKLOADS))
     ap.add_argument("--decode-only", action="store_true",
                     help="only call the decode warmup + steps times (for ncu captures)")
+    ap.add_argument("--eager", action="store_true", help="time eager library calls instead of graph replays")
+    ap.add_argument("--headline-only", action="store_true",
+                    help="skip the other workloads and the combine sweep")
     args = ap.parse_args(argv)
     spec = wl.DECODE_WORKLOADS[args.workload]
     if args.decode_only:

@@ -160,6 +160,40 @@ def _need(t: torch.Tensor, name: str, dtype, contiguous=True):
         raise ValueError("%s must be contiguous" % name)
 
 
+def _decode_geometry(q, kv_cache, block_table, seq_lens, query_start_loc, O_part, lse_part, D: int):
+    """Validate the decode arguments both decode entry points share and
+    return (B, T, H).  Every size the kernels index by is checked here,
+    because the C ABI receives bare pointers: a short block table or a
+    flattened cache would otherwise be read past its end on the device.
+    Shapes are checked before devices, so the checks run on any host."""
+    args = (("q", q, torch.bfloat16, False), ("kv_cache", kv_cache, torch.bfloat16, True),
+            ("block_table", block_table, torch.int32, False), ("seq_lens", seq_lens, torch.int32, True),
+            ("query_start_loc", query_start_loc, torch.int32, True), ("O_part", O_part, torch.float32, True),
+            ("lse_part", lse_part, torch.float32, True))
+    for name, t, dtype, _ in args:
+        if not isinstance(t, torch.Tensor):
+            raise TypeError("%s must be a torch.Tensor" % name)
+        if t.dtype != dtype:
+            raise TypeError("%s must be %s, got %s" % (name, dtype, t.dtype))
+    if q.dim() != 3 or q.shape[2] != KV_DIM or q.stride(2) != 1 or q.stride(1) != KV_DIM:
+        raise ValueError("q must be [T, H, 576] with contiguous heads")
+    if kv_cache.dim() != 3 or kv_cache.shape[2] != KV_DIM:
+        raise ValueError("kv_cache must be [num_blocks, block_size, 576]")
+    if block_table.dim() != 2 or block_table.stride(1) != 1:
+        raise ValueError("block_table must be [B, W] with unit column stride")
+    if seq_lens.dim() != 1 or query_start_loc.dim() != 1:
+        raise ValueError("seq_lens and query_start_loc must be 1-D")
+    T, H = q.shape[0], q.shape[1]
+    B = seq_lens.shape[0]
+    if query_start_loc.shape[0] != B + 1 or block_table.shape[0] != B:
+        raise ValueError("seq_lens [B], query_start_loc [B + 1] and block_table [B, W] disagree on B")
+    if tuple(O_part.shape) != (D, T, H, LATENT_DIM) or tuple(lse_part.shape) != (D, T, H):
+        raise ValueError("O_part must be [D, T, H, 512] and lse_part [D, T, H]")
+    for name, t, dtype, contiguous in args:
+        _need(t, name, dtype, contiguous=contiguous)
+    return B, T, H
+
+
 # ----------------------------------------------------------------------------
 # entry points with the C names
 # ----------------------------------------------------------------------------
@@ -202,25 +236,7 @@ def dcp_mla_decode_partial(q, kv_cache, block_table, seq_lens, query_start_loc, 
     block_table int32 [B, W] (rows may be strided), seq_lens int32 [B],
     query_start_loc int32 [B + 1]; writes O_part fp32 [D, T, H, 512] and
     lse_part fp32 [D, T, H]."""
-    _need(q, "q", torch.bfloat16, contiguous=False)
-    if q.dim() != 3 or q.shape[2] != KV_DIM or q.stride(2) != 1 or q.stride(1) != KV_DIM:
-        raise ValueError("q must be [T, H, 576] with contiguous heads")
-    _need(kv_cache, "kv_cache", torch.bfloat16)
-    if kv_cache.dim() != 3 or kv_cache.shape[2] != KV_DIM:
-        raise ValueError("kv_cache must be [num_blocks, block_size, 576]")
-    _need(block_table, "block_table", torch.int32, contiguous=False)
-    if block_table.dim() != 2 or block_table.stride(1) != 1:
-        raise ValueError("block_table must be [B, W] with unit column stride")
-    _need(seq_lens, "seq_lens", torch.int32)
-    _need(query_start_loc, "query_start_loc", torch.int32)
-    _need(O_part, "O_part", torch.float32)
-    _need(lse_part, "lse_part", torch.float32)
-    T, H = q.shape[0], q.shape[1]
-    B = seq_lens.shape[0]
-    if query_start_loc.shape[0] != B + 1 or block_table.shape[0] != B:
-        raise ValueError("seq_lens, query_start_loc and block_table disagree on B")
-    if tuple(O_part.shape) != (D, T, H, LATENT_DIM) or tuple(lse_part.shape) != (D, T, H):
-        raise ValueError("O_part must be [D, T, H, 512] and lse_part [D, T, H]")
+    B, T, H = _decode_geometry(q, kv_cache, block_table, seq_lens, query_start_loc, O_part, lse_part, D)
     _need_opt(workspace, "workspace", allow_empty=True)
     if workspace is not None and workspace.numel() == 0:
         workspace = None
@@ -243,21 +259,7 @@ def dcp_mla_decode_partial_noalloc(q, kv_cache, block_table, seq_lens, query_sta
     is a fixed 24 MiB array inside the library (shared by all calls, so calls
     that overlap on the GPU race; the first call on a device must precede
     any stream capture on it)."""
-    _need(q, "q", torch.bfloat16, contiguous=False)
-    if q.dim() != 3 or q.shape[2] != KV_DIM or q.stride(2) != 1 or q.stride(1) != KV_DIM:
-        raise ValueError("q must be [T, H, 576] with contiguous heads")
-    _need(kv_cache, "kv_cache", torch.bfloat16)
-    _need(block_table, "block_table", torch.int32, contiguous=False)
-    if block_table.dim() != 2 or block_table.stride(1) != 1:
-        raise ValueError("block_table must be [B, W] with unit column stride")
-    _need(seq_lens, "seq_lens", torch.int32)
-    _need(query_start_loc, "query_start_loc", torch.int32)
-    _need(O_part, "O_part", torch.float32)
-    _need(lse_part, "lse_part", torch.float32)
-    T, H = q.shape[0], q.shape[1]
-    B = seq_lens.shape[0]
-    if tuple(O_part.shape) != (D, T, H, LATENT_DIM) or tuple(lse_part.shape) != (D, T, H):
-        raise ValueError("O_part must be [D, T, H, 512] and lse_part [D, T, H]")
+    B, T, H = _decode_geometry(q, kv_cache, block_table, seq_lens, query_start_loc, O_part, lse_part, D)
     _need_opt(dev_error, "dev_error", torch.int32)
     with _Range("dcp_mla_decode_partial_noalloc"):
         st = lib().dcp_mla_decode_partial_noalloc(
@@ -270,25 +272,42 @@ def dcp_mla_decode_partial_noalloc(q, kv_cache, block_table, seq_lens, query_sta
 
 def dcp_lse_combine(O_part, lse_part, seq_lens, query_start_loc, out, out_lse, *, stream=None) -> None:
     """O_part fp32 [D, T, H, 512], lse_part fp32 [D, T, H] -> out [T, H, 512]
-    (bf16 or fp32, by out.dtype) and out_lse fp32 [T, H]."""
-    _need(O_part, "O_part", torch.float32)
-    _need(lse_part, "lse_part", torch.float32)
-    _need(seq_lens, "seq_lens", torch.int32)
-    _need(query_start_loc, "query_start_loc", torch.int32)
-    _need(out_lse, "out_lse", torch.float32, contiguous=False)
+    (bf16 or fp32, by out.dtype) and out_lse fp32 [T, H].  Shapes are checked
+    (on any host) before devices: the kernel reads D*T*H*512 floats of O_part
+    and indexes query_start_loc up to B."""
+    args = (("O_part", O_part, torch.float32), ("lse_part", lse_part, torch.float32),
+            ("seq_lens", seq_lens, torch.int32), ("query_start_loc", query_start_loc, torch.int32),
+            ("out_lse", out_lse, torch.float32))
+    for name, t, dtype in args:
+        if not isinstance(t, torch.Tensor):
+            raise TypeError("%s must be a torch.Tensor" % name)
+        if t.dtype != dtype:
+            raise TypeError("%s must be %s, got %s" % (name, dtype, t.dtype))
+    if not isinstance(out, torch.Tensor):
+        raise TypeError("out must be a torch.Tensor")
     if out.dtype == torch.bfloat16:
         dt = DTYPE_BF16
     elif out.dtype == torch.float32:
         dt = DTYPE_F32
     else:
         raise TypeError("out must be bfloat16 or float32")
-    _need(out, "out", out.dtype)
+    if lse_part.dim() != 3:
+        raise ValueError("lse_part must be [D, T, H]")
     D, T, H = lse_part.shape
+    if tuple(O_part.shape) != (D, T, H, LATENT_DIM):
+        raise ValueError("O_part must be [D, T, H, 512] with lse_part [D, T, H]")
     if tuple(out.shape) != (T, H, LATENT_DIM) or tuple(out_lse.shape) != (T, H):
         raise ValueError("out must be [T, H, 512] and out_lse [T, H]")
+    if seq_lens.dim() != 1 or query_start_loc.dim() != 1:
+        raise ValueError("seq_lens and query_start_loc must be 1-D")
+    B = seq_lens.shape[0]
+    if query_start_loc.shape[0] != B + 1:
+        raise ValueError("query_start_loc must have B + 1 = %d entries" % (B + 1))
+    for name, t, dtype in args:
+        _need(t, name, dtype, contiguous=name != "out_lse")
+    _need(out, "out", out.dtype)
     if not (out_lse.is_contiguous() or out_lse.data_ptr() == lse_part.data_ptr()):
         raise ValueError("out_lse must be contiguous")
-    B = seq_lens.shape[0]
     with _Range("dcp_lse_combine"):
         st = lib().dcp_lse_combine(_ptr(O_part), _ptr(lse_part), _ptr(seq_lens), _ptr(query_start_loc), B, T,
                                    H, D, _ptr(out), dt, _ptr(out_lse), _stream(stream))

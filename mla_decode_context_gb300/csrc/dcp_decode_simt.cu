@@ -11,6 +11,7 @@
 #include "dcp_kernels.h"
 
 #include <cmath>
+#include <mutex>
 
 namespace dcp {
 namespace {
@@ -165,9 +166,21 @@ decode_simt_kernel(DecodeArgs a) {
 
 cudaError_t launch_decode_simt(const DecodeArgs& a, cudaStream_t st) {
   const size_t smem = sizeof(Smem);
-  cudaError_t e = cudaFuncSetAttribute(decode_simt_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(smem));
-  if (e != cudaSuccess) return e;
+  // shared-memory opt-in once per device (not per launch: launches may be
+  // captured into a CUDA graph)
+  static std::mutex mu;
+  static bool done[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    if (!done[dev]) {
+      cudaError_t e = cudaFuncSetAttribute(decode_simt_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           static_cast<int>(smem));
+      if (e != cudaSuccess) return e;
+      done[dev] = true;
+    }
+  }
   const int64_t gx = static_cast<int64_t>((a.H + kHeadsPerCta - 1) / kHeadsPerCta) * a.T;
   const int64_t gy = static_cast<int64_t>(a.D) * a.plan.splits;
   if (gx > 0x7fffffffLL || gy > 65535) return cudaErrorInvalidConfiguration;

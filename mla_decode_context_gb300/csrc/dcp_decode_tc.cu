@@ -68,6 +68,7 @@
 
 #include <cmath>
 #include <cstring>
+#include <mutex>
 
 namespace dcp {
 namespace {
@@ -553,17 +554,22 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(DecodeArgs a) {
         f2_unpack(f2_add(f2_pack(sc[2 * i], sc[2 * i + 1]),
                          f2_pack(__uint_as_float(sr[2 * i]), __uint_as_float(sr[2 * i + 1]))),
                   sc[2 * i], sc[2 * i + 1]);
-      // online softmax (base 2); masked tokens get weight 0 by selection
+      // online softmax in base 2: x = s * scale * log2(e), scaled before the
+      // mask and the max so that any finite scale (zero and negative too)
+      // keeps masked tokens at -inf; masked tokens get weight 0 by selection
+      const uint64_t sl2x2 = f2_pack(sl2, sl2);
+#pragma unroll
+      for (int i = 0; i < 16; ++i) f2_unpack(f2_mul(f2_pack(sc[2 * i], sc[2 * i + 1]), sl2x2), sc[2 * i], sc[2 * i + 1]);
       if (mask != 0xffffffffu) {
 #pragma unroll
         for (int i = 0; i < 32; ++i) sc[i] = (mask >> i) & 1u ? sc[i] : -INFINITY;
       }
-      // row max of the raw scores (scale > 0 commutes with max), as a tree
+      // row max, as a tree
       float mx[8];
 #pragma unroll
       for (int i = 0; i < 8; ++i) mx[i] = fmaxf(fmaxf(sc[4 * i], sc[4 * i + 1]), fmaxf(sc[4 * i + 2], sc[4 * i + 3]));
       const float tmax = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                               fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))) * sl2;
+                               fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
       // adopt the other group's max if it is larger (it only grows)
       if (m_other > m_used) {
         if (m_used != -INFINITY) l_sum *= ex2_approx(m_used - m_other);
@@ -579,16 +585,16 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(DecodeArgs a) {
       m_ring[(j & 7) * 128 + h] = m_used;
       __syncwarp();
       if (lane == 0) mbar_arrive(&bar.m_pub[j & 7]);
-      // p = 2^(s * scale * log2e - m); masked (-inf) scores give exactly 0,
-      // and nothing is live while m is still -inf
+      // p = 2^(x - m); masked (-inf) scores give exactly 0, and nothing is
+      // live while m is still -inf
       const float nm = m_used == -INFINITY ? 0.f : -m_used;
-      const uint64_t sl2x2 = f2_pack(sl2, sl2), nmx2 = f2_pack(nm, nm);
+      const uint64_t nmx2 = f2_pack(nm, nm);
       uint32_t pk[16];
       uint64_t ps[2] = {f2_pack(0.f, 0.f), f2_pack(0.f, 0.f)};
 #pragma unroll
       for (int i = 0; i < 16; ++i) {
         float e0, e1;
-        f2_unpack(f2_fma(f2_pack(sc[2 * i], sc[2 * i + 1]), sl2x2, nmx2), e0, e1);
+        f2_unpack(f2_add(f2_pack(sc[2 * i], sc[2 * i + 1]), nmx2), e0, e1);
         const float p0 = ex2_approx(e0), p1 = ex2_approx(e1);
         __nv_bfloat162 pb = __floats2bfloat162_rn(p0, p1);  // P feeds the PV MMA in bf16
         ps[i & 1] = f2_add(ps[i & 1], f2_pack(p0, p1));     // l (hence the LSE) stays fp32
@@ -861,13 +867,22 @@ cudaLaunchConfig_t launch_config(int64_t units, cudaStream_t st, cudaLaunchAttri
 
 }  // namespace
 
-int decode_tc_resident_ctas() {
-  // CTAs of the tensor-core decode that fit on the current device at once
-  // (1 per SM by shared memory; clusters of two must sit in one GPC).
-  static int cached_dev = -1, cached = 0;
+namespace {
+// Per-device one-time set-up of the tensor-core decode: its shared-memory
+// opt-in and the number of its clusters that fit on the device at once.  One
+// entry per device, behind a mutex, so that concurrent host threads and
+// alternating devices always size the split plan from the same count, and a
+// launch (possibly inside a stream capture) makes no attribute call.
+constexpr int kMaxDevices = 64;
+std::mutex g_setup_mu;
+int g_resident[kMaxDevices] = {};  // 0: not yet set up
+
+int setup_current_device() {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) { cudaGetLastError(); return 0; }
-  if (dev == cached_dev) return cached;
+  if (dev < 0 || dev >= kMaxDevices) return 0;
+  std::lock_guard<std::mutex> lock(g_setup_mu);
+  if (g_resident[dev] > 0) return g_resident[dev];
   if (cudaFuncSetAttribute(decode_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) !=
       cudaSuccess) { cudaGetLastError(); return 0; }
   cudaLaunchAttribute attr[1];
@@ -877,9 +892,15 @@ int decode_tc_resident_ctas() {
     cudaGetLastError();
     return 0;
   }
-  cached_dev = dev;
-  cached = 2 * clusters;
-  return cached;
+  g_resident[dev] = 2 * clusters;
+  return g_resident[dev];
+}
+}  // namespace
+
+int decode_tc_resident_ctas() {
+  // CTAs of the tensor-core decode that fit on the current device at once
+  // (1 per SM by shared memory; clusters of two must sit in one GPC).
+  return setup_current_device();
 }
 
 cudaError_t launch_unit_order(const DecodeArgs& a, int32_t units, int32_t* order, cudaStream_t st) {
@@ -896,8 +917,7 @@ bool decode_tc_supported(const DecodeArgs& a) {
 
 cudaError_t launch_decode_tc(const DecodeArgs& a, cudaStream_t st) {
   if (!decode_tc_supported(a)) return cudaErrorInvalidValue;
-  cudaError_t e = cudaFuncSetAttribute(decode_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-  if (e != cudaSuccess) return e;
+  if (setup_current_device() <= 0) return cudaErrorInvalidDevice;
   const int64_t units = static_cast<int64_t>(a.T) * a.D * a.plan.splits;
   if (2 * units > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
   cudaLaunchAttribute attr[1];

@@ -132,3 +132,72 @@ def test_nvtx_range_never_raises():
     # GPU or NVTX the range must be a no-op, never an error
     with dcp._Range("dcp_test_range"):
         pass
+
+
+NOALLOC_SCRATCH_BYTES = 24 << 20
+
+
+def test_noalloc_scratch_covers_every_128_head_plan(L):
+    """The allocation-free decode's fixed scratch (24 MiB) covers every split
+    plan with H = 128 heads at the sizes the library is used at (sized here
+    for a 152-SM GB300, the count used when no device is visible)."""
+    for D in range(1, 33):
+        for T in list(range(1, 65)) + [128, 256, 1024, 2048, 4096]:
+            for msl in (1, 255, 256, 4096, 32768, 120000, 1 << 20):
+                n = dcp.dcp_decode_workspace_size(T, T, 128, D, msl, 4)
+                assert n <= NOALLOC_SCRATCH_BYTES, (D, T, msl, n)
+
+
+def test_noalloc_refuses_a_plan_beyond_its_scratch(L):
+    """1024 heads over a 120,000-token context need ~150 MB of split partials:
+    refused with DCP_ERR_WORKSPACE_TOO_SMALL before anything is launched
+    (the pointers here are never dereferenced)."""
+    f = L.dcp_mla_decode_partial_noalloc
+    st = f(0x1000, 1024 * 576, 0x2000, 1875, 64, 0x3000, 1875, 1875, 0x4000, 0x5000, 1, 1, 1024, 120000, 1,
+           8, 1, 0.07, 0x6000, 0x7000, None, None)
+    assert st == 5
+
+
+def _cpu_decode_args(**kw):
+    import torch
+    a = dict(q=torch.zeros((2, 16, 576), dtype=torch.bfloat16), kv=torch.zeros((4, 16, 576), dtype=torch.bfloat16),
+             tab=torch.zeros((2, 4), dtype=torch.int32), seq=torch.zeros(2, dtype=torch.int32),
+             qsl=torch.zeros(3, dtype=torch.int32), O=torch.zeros((4, 2, 16, 512)), lse=torch.zeros((4, 2, 16)))
+    a.update(kw)
+    return a
+
+
+@pytest.mark.parametrize("entry", ["dcp_mla_decode_partial", "dcp_mla_decode_partial_noalloc"])
+def test_decode_wrappers_check_shapes_before_the_device(entry):
+    """Both decode wrappers reject, with ValueError and before touching a
+    device, the shapes the C ABI cannot see: a block table with fewer than B
+    rows, a flattened cache, a query_start_loc without B + 1 entries."""
+    import torch
+    f = getattr(dcp, entry)
+
+    def call(a):
+        f(a["q"], a["kv"], a["tab"], a["seq"], a["qsl"], a["O"], a["lse"], D=4, interleave=1, scale=0.1,
+          max_seq_len=37, max_q_len=1)
+    for bad, msg in ((dict(tab=torch.zeros((1, 4), dtype=torch.int32)), "disagree on B"),
+                     (dict(kv=torch.zeros((64, 576), dtype=torch.bfloat16)), "kv_cache"),
+                     (dict(qsl=torch.zeros(2, dtype=torch.int32)), "disagree on B"),
+                     (dict(O=torch.zeros((4, 2, 16, 256))), "O_part")):
+        with pytest.raises(ValueError, match=msg):
+            call(_cpu_decode_args(**bad))
+    with pytest.raises(ValueError, match="CUDA tensor"):  # right shapes, host memory
+        call(_cpu_decode_args())
+
+
+def test_combine_wrapper_checks_shapes_before_the_device():
+    import torch
+    O, lse = torch.zeros((4, 2, 16, 512)), torch.zeros((4, 2, 16))
+    seq, qsl = torch.zeros(2, dtype=torch.int32), torch.zeros(3, dtype=torch.int32)
+    out, out_lse = torch.zeros((2, 16, 512), dtype=torch.bfloat16), torch.zeros((2, 16))
+    with pytest.raises(ValueError, match="O_part"):
+        dcp.dcp_lse_combine(torch.zeros((4, 2, 16, 500)), lse, seq, qsl, out, out_lse)
+    with pytest.raises(ValueError, match="O_part"):
+        dcp.dcp_lse_combine(torch.zeros((3, 2, 16, 512)), lse, seq, qsl, out, out_lse)
+    with pytest.raises(ValueError, match="B \\+ 1"):
+        dcp.dcp_lse_combine(O, lse, seq, torch.zeros(2, dtype=torch.int32), out, out_lse)
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        dcp.dcp_lse_combine(O, lse, seq, qsl, out, out_lse)

@@ -138,7 +138,7 @@ def _fill_request(kv_flat: np.ndarray, phys_rows: np.ndarray, spec: DecodeSpec,
             list(ex.map(work, jobs))
 
 
-def make_decode_inputs(spec: DecodeSpec) -> dict:
+def make_decode_inputs(spec: DecodeSpec, kv_rows=None) -> dict:
     """Host (numpy) inputs of one decode workload.
 
     Returns a dict with ``q`` uint16 [T, H, 576] (bf16 bits), ``kv_cache``
@@ -146,6 +146,11 @@ def make_decode_inputs(spec: DecodeSpec) -> dict:
     ``seq_lens`` int32 [B], ``query_start_loc`` int32 [B + 1] and the scalar
     parameters (``T``, ``H``, ``D``, ``interleave``, ``block_size``,
     ``scale``, ``max_seq_len``, ``max_q_len``).
+
+    ``kv_rows(b, positions)``, when given, supplies the bf16 bits
+    (uint16 [len(positions), 576]) of request b's latent rows at those
+    logical positions instead of the seeded normal draws (for tests that
+    plant known values, e.g. rows that encode their own position).
     """
     seq = spec.resolved_seq_lens()
     qlens = np.asarray(spec.q_lens(), dtype=np.int32)
@@ -178,7 +183,10 @@ def make_decode_inputs(spec: DecodeSpec) -> dict:
             continue
         pos = np.arange(L, dtype=np.int64)
         phys = table[b, pos // bs].astype(np.int64) * bs + pos % bs
-        _fill_request(kv_flat, phys, spec, b, L)
+        if kv_rows is None:
+            _fill_request(kv_flat, phys, spec, b, L)
+        else:
+            kv_flat[phys] = kv_rows(b, pos)
 
     q = f32_to_bf16_bits(np.random.default_rng([spec.seed, _S_Q]).standard_normal(
         (T, spec.H, KDIM), dtype=np.float32))
