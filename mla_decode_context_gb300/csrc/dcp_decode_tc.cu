@@ -105,7 +105,8 @@ constexpr uint32_t kTmemCols = 512;
 struct __align__(8) Bars {
   uint64_t kv_loaded[kStages];  // score: own rows of tile j landed (every thread of tile j's producer group)
   // kv_full (score): the whole tile j is in its stage for S: the value CTA's
-  // 16 KB landed (armed by a producer) and the forwarder has made this CTA's
+  // 16 KB landed (armed by a producer), the four producer warps of the tile
+  // wrote their bytes of its row mask, and the forwarder has made this CTA's
   // own rows visible to the tensor cores
   uint64_t kv_full[kStages];
   // s_done (both CTAs): the score CTA's stage of tile j is free again: all
@@ -132,6 +133,9 @@ struct __align__(8) Bars {
   uint64_t fin_l;             // value: 1/l of every head arrived from the score CTA
   uint64_t fin[1 + kSParts * kSBuf];  // each issuing warp's MMAs complete
   uint64_t m_pub[8];          // score: running max after tile j posted (phase j / 8 of m_pub[j % 8]; 4 warps)
+  // score: the other group has read the max posted after tile k (phase k / 8
+  // of m_read[k % 8]; 4 warps): slot k % 8 may take tile k + 8's max
+  uint64_t m_read[8];
   uint64_t sm_fin;            // score: both softmax groups' final l and m written (8 warps)
   uint64_t never;             // test hook only: initialised, never arrived on
   // score: valid rows of tile j in mask[j % 16] (written by the producer
@@ -152,8 +156,81 @@ constexpr int kOffSm = kOffFin + 512;                    // score: running max p
 constexpr int kOffBars = kOffSm + 12 * 128 * 4;
 constexpr int kSmemBytes = kOffBars + static_cast<int>(sizeof(Bars)) + 1024;  // + alignment slack
 static_assert(kSmemBytes <= 232448, "exceeds the 227 KB of shared memory per CTA");
+
+// Score CTA stage ring: chunk c of stage st (32 rows x 128 B, 128B-swizzled).
+__host__ __device__ constexpr int stage_chunk_off(int st, int c) { return kOffStages + st * kStageBytes + c * kChunkBytes; }
 static_assert(kPSlotBytes % 1024 == 0 && kOffP % 1024 == 0, "P tiles must sit on swizzle-atom boundaries");
 static_assert(kOffRecv + kRecv * kHalfBytes <= kOffP, "value CTA rings overlap the P slots");
+
+// Cycle accounting for performance work, compiled only with -DDCP_TRACE=R
+// (never in the library build): the warps of role R (1 producers, 2 score
+// forwarder, 3 S issuers, 4 softmax, 6 value forwarder, 7 receive warp, 8 PV
+// issuer, 9 value max / epilogue warps) add clock64 deltas into eight
+// counters (TR_LAP(R, k): time since the last mark goes to counter k), and
+// lane 0 of every warp of the first kTraceClusters clusters stores them at
+// the end, counter 7 being the warp's whole life.  One role per build keeps
+// the counters out of the other roles' registers.  Every CTA also records
+// its SM and the global timer at entry and at exit.
+#ifdef DCP_TRACE
+constexpr int kTraceClusters = 16;
+constexpr int kTraceCtas = 1024;
+__device__ __align__(16) uint32_t g_dcp_trace[kTraceClusters * 2][32][8];
+__device__ __align__(16) unsigned long long g_dcp_timeline[kTraceCtas][8];  // t_entry, t_exit, smid, unit, clk_entry, clk_exit, t_init
+__device__ __forceinline__ unsigned long long tr_globaltimer() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+#define TR_ENTRY()                                                                      \
+  const unsigned long long tr_entry = threadIdx.x == 0 ? tr_globaltimer() : 0ull;       \
+  const unsigned long long tr_clk_entry = threadIdx.x == 0 ? clock64() : 0ull
+#define TR_INIT()                                                     \
+  if (threadIdx.x == 0 && blockIdx.x < kTraceCtas) g_dcp_timeline[blockIdx.x][6] = tr_globaltimer(); \
+  uint32_t tr_c[8] = {0, 0, 0, 0, 0, 0, 0, 0};                       \
+  const uint32_t tr_start = static_cast<uint32_t>(clock64());         \
+  uint32_t tr_t = tr_start
+#define TR_MARK(r)                                                    \
+  do {                                                                \
+    if ((r) == DCP_TRACE) tr_t = static_cast<uint32_t>(clock64());    \
+  } while (0)
+#define TR_LAP(r, k)                                                  \
+  do {                                                                \
+    if ((r) == DCP_TRACE) {                                           \
+      const uint32_t tr_n = static_cast<uint32_t>(clock64());         \
+      tr_c[k] += tr_n - tr_t;                                         \
+      tr_t = tr_n;                                                    \
+    }                                                                 \
+  } while (0)
+#define TR_DUMP()                                                                               \
+  do {                                                                                          \
+    if (blockIdx.x < 2 * kTraceClusters && (threadIdx.x & 31) == 0) {                           \
+      tr_c[7] = static_cast<uint32_t>(clock64()) - tr_start;                                    \
+      uint4* tr_d = reinterpret_cast<uint4*>(&g_dcp_trace[blockIdx.x][threadIdx.x >> 5][0]);     \
+      tr_d[0] = make_uint4(tr_c[0], tr_c[1], tr_c[2], tr_c[3]);                                 \
+      tr_d[1] = make_uint4(tr_c[4], tr_c[5], tr_c[6], tr_c[7]);                                 \
+    }                                                                                           \
+  } while (0)
+#define TR_EXIT(unit)                                                                           \
+  do {                                                                                          \
+    if (threadIdx.x == 0 && blockIdx.x < kTraceCtas) {                                          \
+      uint32_t smid;                                                                            \
+      asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));                                         \
+      g_dcp_timeline[blockIdx.x][0] = tr_entry;                                                 \
+      g_dcp_timeline[blockIdx.x][1] = tr_globaltimer();                                         \
+      g_dcp_timeline[blockIdx.x][2] = smid;                                                     \
+      g_dcp_timeline[blockIdx.x][3] = static_cast<unsigned long long>(unit);                    \
+      g_dcp_timeline[blockIdx.x][4] = tr_clk_entry;                                             \
+      g_dcp_timeline[blockIdx.x][5] = clock64();                                                \
+    }                                                                                           \
+  } while (0)
+#else
+#define TR_ENTRY() do {} while (0)
+#define TR_INIT() do {} while (0)
+#define TR_MARK(r) do {} while (0)
+#define TR_LAP(r, k) do {} while (0)
+#define TR_DUMP() do {} while (0)
+#define TR_EXIT(unit) do {} while (0)
+#endif
 
 __device__ __forceinline__ void report(int32_t* dev_error, uint32_t bits) {
   if (dev_error) atomicOr(dev_error, static_cast<int32_t>(bits));
@@ -168,6 +245,7 @@ __device__ __forceinline__ void set_abort(Bars& bar, int32_t* dev_error) {
 
 __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(DecodeArgs a) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
+  TR_ENTRY();
   unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                          ~static_cast<uintptr_t>(1023));
   Bars& bar = *reinterpret_cast<Bars*>(smem + kOffBars);
@@ -203,14 +281,31 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(DecodeArgs a) {
         }
       }
     }
+    TR_EXIT(unit);
     return;
+  }
+
+  if (score && warp < 8) {
+    // Q load, issued before the set-up below so that its latency overlaps
+    // it.  The 147 KB of Q (128 heads x 576 dims, the same for every unit of
+    // a row) come in with one round of cp.async into stages 0-3 (unused until
+    // Q is in TMEM): head h at 1152 h, its 16-byte unit u at position
+    // u ^ (h & 7) within each 8-unit group.  Heads h >= H are zero.
+    const unsigned char* qb = reinterpret_cast<const unsigned char*>(a.q + static_cast<int64_t>(r) * a.q_stride_tok);
+    const uint32_t qs = smem_u32(smem) + kOffStages;
+    for (int p = threadIdx.x; p < 128 * 72; p += 256) {
+      const int hh = p / 72, u = p - hh * 72;
+      const int us = (u & ~7) | ((u & 7) ^ (hh & 7));
+      cp_async16_zfill(qs + hh * 1152 + us * 16, qb + (hh < a.H ? hh : 0) * 1152 + u * 16, hh < a.H ? 16u : 0u);
+    }
+    cp_async_commit();
   }
 
   // ---------------------------------------------------------------- setup
   if (threadIdx.x == 0) {
     for (int i = 0; i < kStages; ++i) {
       mbar_init(&bar.kv_loaded[i], kGroupThreads);
-      mbar_init(&bar.kv_full[i], 2);
+      mbar_init(&bar.kv_full[i], 5);  // 4 producer warps of the tile's group + the forwarder
       mbar_init(&bar.s_done[i], kSParts + 1);
     }
     for (int i = 0; i < kOwn; ++i) { mbar_init(&bar.own_loaded[i], kGroupThreads); mbar_init(&bar.own_free[i], 1); }
@@ -228,7 +323,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(DecodeArgs a) {
     mbar_init(&bar.o_final, 1);
     mbar_init(&bar.fin_l, 1);
     for (int i = 0; i < 1 + kSParts * kSBuf; ++i) mbar_init(&bar.fin[i], 1);
-    for (int i = 0; i < 8; ++i) mbar_init(&bar.m_pub[i], 4);
+    for (int i = 0; i < 8; ++i) { mbar_init(&bar.m_pub[i], 4); mbar_init(&bar.m_read[i], 4); }
     mbar_init(&bar.sm_fin, 8);
     mbar_init(&bar.never, 1);
     bar.abort = 0;
@@ -249,22 +344,12 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(DecodeArgs a) {
   cluster_sync();  // peer's barriers initialised and armed before any remote operation
   tc_fence_after();
   const uint32_t tbase = bar.tmem;
+  TR_INIT();
   if (score && warp < 8) {
-    // Q -> TMEM.  The 147 KB of Q (128 heads x 576 dims, the same for every
-    // unit of a row) come in with one round of cp.async into stages 0-3
-    // (unused until Q is in TMEM): head h at 1152 h, its 16-byte unit u at
-    // position u ^ (h & 7) within each 8-unit group.  Then thread = head =
-    // lane of the warp's lane quarter moves its row to TMEM (warps 0-3 the
-    // even chunks, 4-7 the odd ones): dim k goes to column k / 2 (low half =
-    // even k).  Heads h >= H are zero.
-    const unsigned char* qb = reinterpret_cast<const unsigned char*>(a.q + static_cast<int64_t>(r) * a.q_stride_tok);
-    const uint32_t qs = smem_u32(smem) + kOffStages;
-    for (int p = threadIdx.x; p < 128 * 72; p += 256) {
-      const int hh = p / 72, u = p - hh * 72;
-      const int us = (u & ~7) | ((u & 7) ^ (hh & 7));
-      cp_async16_zfill(qs + hh * 1152 + us * 16, qb + (hh < a.H ? hh : 0) * 1152 + u * 16, hh < a.H ? 16u : 0u);
-    }
-    cp_async_commit();
+    // Q -> TMEM, once the copies issued before the set-up have landed:
+    // thread = head = lane of the warp's lane quarter moves its row to TMEM
+    // (warps 0-3 the even chunks, 4-7 the odd ones): dim k goes to column
+    // k / 2 (low half = even k).
     cp_async_wait<0>();
     mbar_arrive(&bar.q_staged);
     const bool staged = __all_sync(0xffffffffu, mbar_wait(&bar.q_staged, 0));
@@ -287,6 +372,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(DecodeArgs a) {
     tc_fence_before();
     __syncwarp();
     if (lane == 0) mbar_arrive(&bar.q_ready);
+    TR_LAP(4, 6);  // score warps 0-7: Q load
   }
 
   const int32_t* trow = a.block_table + static_cast<int64_t>(ri.b) * a.bt_stride;
@@ -296,72 +382,97 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(DecodeArgs a) {
   if (warp >= kProdWarp0 && warp < kSmWarp1) {
     // ----------------------------------------------------------- producers
     // Two groups of four warps take alternate tiles (a producer thread's
-    // issue is latency-bound, so two tiles are in flight at once).  The 128
-    // threads of a group copy the 16-byte units of the CTA's own chunks of
-    // the tile's rows (upr units per row: chunks 0-3 + 8 = 40 into the
-    // score CTA's stage, chunks 4-7 = 32 into the value CTA's own slot, laid
-    // out as the stage's chunks 4-7 are); unit p = i * 128 + t, so
-    // consecutive lanes read consecutive bytes of a row.  Lane i of each
-    // warp resolves row i of the tile (shard token -> cache row), one of
-    // the group's tiles ahead.  Each thread's copies of a tile arrive on
-    // kv_loaded / own_loaded by themselves when they complete; the
-    // consumers fence them into the async proxy.
+    // issue is latency-bound, so two tiles are in flight at once).  Warp gw
+    // of a group owns rows 8 gw .. 8 gw + 7 of the tile, four at a time:
+    // eight lanes per row, lane x copying the x-th 16-byte unit of every
+    // chunk the CTA loads itself (chunks 0-3 and the rope chunk 8 into the
+    // score CTA's stage, chunks 4-7 into the value CTA's own slot, laid out
+    // as the stage's chunks are), so each copy instruction reads four whole
+    // 128-byte lines.  Each thread resolves its own two rows (shard token ->
+    // cache row) one of the group's tiles ahead: no values move between
+    // lanes, which keeps the SM's memory-instruction queue, busy with the
+    // copies, free of shuffles.  Each thread's copies of a tile arrive on
+    // kv_loaded / own_loaded by themselves when they complete; the consumers
+    // fence them into the async proxy.
     const int group = (warp - kProdWarp0) >> 2;
-    const bool leader = ((warp - kProdWarp0) & 3) == 0;  // first warp of the group
-    const int t = (warp - kProdWarp0 - 4 * group) * 32 + lane;
-    const int upr = score ? 40 : 32;
-    const int per_thread = kTile * upr / kGroupThreads;
+    const int gw = (warp - kProdWarp0) & 3;
+    const int x = lane & 7;
+    const int row0 = 8 * gw + (lane >> 3), row1 = row0 + 4;
+    const int nch = score ? 5 : 4;  // chunks this CTA loads itself
     const unsigned char* kvb = reinterpret_cast<const unsigned char*>(a.kv);
     uint64_t* own_free = score ? bar.s_done : bar.own_free;
     uint64_t* own_loaded = score ? bar.kv_loaded : bar.own_loaded;
     const int nslots = score ? kStages : kOwn;
     const int32_t DI = a.D * a.I, dI = d * a.I;
-    bool in_n = false;
-    int32_t pos_n = 0, blk_n = -1;
+    bool in_n[2] = {false, false};
+    int32_t pos_n[2] = {0, 0}, blk_n[2] = {-1, -1};
     auto fetch = [&](int jj) {  // positions fit in 32 bits (seq_lens are int32)
-      const int32_t l = lo + jj * kTile + lane;
-      in_n = l < hi;
-      pos_n = in_n ? (l / a.I) * DI + dI + l % a.I : 0;
-      blk_n = in_n ? __ldg(trow + pos_n / a.block_size) : -1;
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const int32_t l = lo + jj * kTile + (e ? row1 : row0);
+        in_n[e] = l < hi;
+        pos_n[e] = in_n[e] ? (l / a.I) * DI + dI + l % a.I : 0;
+        blk_n[e] = in_n[e] ? __ldg(trow + pos_n[e] / a.block_size) : -1;
+      }
     };
     fetch(group);
     bool ok = true;
     if (score) ok = __all_sync(0xffffffffu, mbar_wait(&bar.q_ready, 0));
+    TR_LAP(1, 5);  // producers: waiting for Q to leave the stages
     for (int j = group; j < ntiles && ok; j += 2) {
-      const bool in = in_n;
-      const int32_t pos = pos_n, blk = blk_n;
+      bool valid[2];
+      int32_t crow[2];
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        valid[e] = in_n[e] && blk_n[e] >= 0 && blk_n[e] < a.num_blocks;
+        // cache row (fits in 31 bits: the library only takes caches of < 2^31 rows)
+        crow[e] = valid[e] ? blk_n[e] * a.block_size + pos_n[e] % a.block_size : 0;
+      }
+      const bool bad = (in_n[0] && !valid[0]) || (in_n[1] && !valid[1]);
       if (j + 2 < ntiles) fetch(j + 2);
       const int st = j % nslots;
       // the abort flag is read here and tested after this tile's copies are
       // issued, so that its shared-memory latency overlaps them
       const bool ab = aborted(bar);
+      TR_LAP(1, 2);  // producers: block ids, loop
       ok = __all_sync(0xffffffffu, mbar_wait(&own_free[st], ((j / nslots) & 1) ^ 1));
+      TR_LAP(1, 0);  // producers: waiting for a free slot
       if (!ok) break;
-      const bool valid = in && blk >= 0 && blk < a.num_blocks;
-      if (in && !valid && score && leader) report(a.dev_error, DCP_DEVERR_BAD_BLOCK);
-      // cache row (fits in 31 bits: the library only takes caches of < 2^31 rows)
-      const int32_t crow = valid ? blk * a.block_size + pos % a.block_size : 0;
-      const uint32_t mask = __ballot_sync(0xffffffffu, valid);
-      if (score && leader && lane == 0) {
-        bar.mask[j & 15] = mask;
-        // tile j - 5 is done with the stage, so kv_full's previous phase is
-        // complete: arm it for the value CTA's 16 KB of tile j
-        mbar_arrive_expect_tx(&bar.kv_full[st], kHalfBytes);
+      if (__any_sync(0xffffffffu, bad) && score && lane == 0) report(a.dev_error, DCP_DEVERR_BAD_BLOCK);
+      if (score) {
+        // this warp's 8 rows of the tile's mask (lanes 8q .. 8q + 7 hold rows
+        // 8 gw + q and 8 gw + 4 + q), then its arrival on kv_full releases
+        // that byte to the softmax; warp 0 of the group also arms kv_full for
+        // the value CTA's 16 KB (tile j - 5 is done with the stage, so its
+        // previous phase is over)
+        const unsigned v0 = __ballot_sync(0xffffffffu, valid[0]), v1 = __ballot_sync(0xffffffffu, valid[1]);
+        if (lane == 0) {
+          uint32_t m8 = 0;
+#pragma unroll
+          for (int q = 0; q < 4; ++q) m8 |= (((v0 >> (8 * q)) & 1u) << q) | (((v1 >> (8 * q)) & 1u) << (4 + q));
+          reinterpret_cast<volatile uint8_t*>(&bar.mask[j & 15])[gw] = static_cast<uint8_t>(m8);
+          if (gw == 0) mbar_arrive_expect_tx(&bar.kv_full[st], kHalfBytes);
+          else mbar_arrive(&bar.kv_full[st]);
+        }
       }
-      // the value CTA's own slot holds chunks 4-7 at chunk offsets 0-3
-      const uint32_t sbase = score ? smem_base + kOffStages + st * kStageBytes
-                                   : smem_base + kOffOwn + st * kHalfBytes - 4 * kChunkBytes;
-#pragma unroll 10
-      for (int i = 0; i < per_thread; ++i) {
-        const int p = i * kGroupThreads + t;
-        const int row = score ? p / 40 : p >> 5;
-        const int u = p - row * upr;
-        const int c = score ? (u < 32 ? (u >> 3) : 8) : 4 + (u >> 3);  // chunk
-        const int64_t ro = static_cast<int64_t>(__shfl_sync(0xffffffffu, crow, row)) * (kKDim * 2);
-        const uint32_t dst = sbase + c * kChunkBytes + row * 128 + (((u & 7) ^ (row & 7)) << 4);
-        cp_async16_zfill(dst, kvb + ro + c * 128 + (u & 7) * 16, ((mask >> row) & 1u) ? 16u : 0u);
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const int row = e ? row1 : row0;
+        const unsigned char* src_row = kvb + static_cast<int64_t>(crow[e]) * (kKDim * 2) + x * 16;
+        const uint32_t src_bytes = valid[e] ? 16u : 0u;
+        const uint32_t swz = static_cast<uint32_t>(row * 128 + ((x ^ (row & 7)) << 4));
+#pragma unroll
+        for (int i = 0; i < nch; ++i) {
+          // score: chunks 0-3, 8 at stage_chunk_off(st, c); value: chunks
+          // 4-7 at its own slot's chunk offsets 0-3
+          const int c = score ? (i < 4 ? i : 8) : 4 + i;
+          const uint32_t dst = score ? smem_base + stage_chunk_off(st, c) + swz
+                                     : smem_base + kOffOwn + st * kHalfBytes + i * kChunkBytes + swz;
+          cp_async16_zfill(dst, src_row + c * 128, src_bytes);
+        }
       }
       cp_async_mbar_arrive_noinc(&own_loaded[st]);
+      TR_LAP(1, 1);  // producers: issuing the copies
       if (__any_sync(0xffffffffu, ab)) {
         ok = false;
         break;
@@ -395,14 +506,15 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(DecodeArgs a) {
       }
       if (jc < jf && __all_sync(0xffffffffu, mbar_peek_cluster(&bar.v_free[jc % kRecv], ((jc / kRecv) & 1) ^ 1))) {
         const int st = jc % kStages, rs = jc % kRecv;
-        if (lane == 0)
-          bulk_copy_to_peer(map_peer(smem_base + kOffRecv + rs * kHalfBytes, peer),
-                            smem + kOffStages + st * kStageBytes, kHalfBytes, map_peer(smem_u32(&bar.v_full[rs]), peer));
+        if (lane == 0)  // chunks 0-3 of the stage -> the receive slot
+          bulk_copy_to_peer(map_peer(smem_base + kOffRecv + rs * kHalfBytes, peer), smem + stage_chunk_off(st, 0),
+                            kHalfBytes, map_peer(smem_u32(&bar.v_full[rs]), peer));
         __syncwarp();
         ++jc;
         moved = true;
       }
       idle = moved ? 0u : idle + 1u;
+      if (moved) TR_LAP(2, 1); else TR_LAP(2, 0);  // forwarder: working / polling
       if (idle > kWaitLimit) ok = false;
     }
     if (!ok) set_abort(bar, a.dev_error);
@@ -411,16 +523,20 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(DecodeArgs a) {
     // Own slot j % kOwn (chunks 4-7) -> the score CTA's stage of tile j, once
     // that stage is free (tile j - 5 done there) and no longer holds Q.
     bool ok = __all_sync(0xffffffffu, mbar_wait_cluster(&bar.q_gone, 0));
+    TR_LAP(6, 5);
     for (int j = 0; j < ntiles && ok; ++j) {
       const int st = j % kStages, os = j % kOwn;
-      ok = __all_sync(0xffffffffu, mbar_wait(&bar.own_loaded[os], (j / kOwn) & 1) &&
-                                       mbar_wait_cluster(&bar.s_done[st], ((j / kStages) & 1) ^ 1));
+      ok = __all_sync(0xffffffffu, mbar_wait(&bar.own_loaded[os], (j / kOwn) & 1));
+      TR_LAP(6, 0);  // value forwarder: waiting for own rows
+      ok = ok && __all_sync(0xffffffffu, mbar_wait_cluster(&bar.s_done[st], ((j / kStages) & 1) ^ 1));
+      TR_LAP(6, 1);  // value forwarder: waiting for the score stage to be free
       if (!ok) break;
       fence_proxy_async_smem();  // the producers' cp.async writes -> the bulk copy
-      if (lane == 0)
-        bulk_copy_to_peer(map_peer(smem_base + kOffStages + st * kStageBytes + 4 * kChunkBytes, peer),
-                          smem + kOffOwn + os * kHalfBytes, kHalfBytes, map_peer(smem_u32(&bar.kv_full[st]), peer));
+      if (lane == 0)  // own chunks 4-7 -> chunks 4-7 of the score CTA's stage
+        bulk_copy_to_peer(map_peer(smem_base + stage_chunk_off(st, 4), peer), smem + kOffOwn + os * kHalfBytes,
+                          kHalfBytes, map_peer(smem_u32(&bar.kv_full[st]), peer));
       __syncwarp();
+      TR_LAP(6, 2);  // value forwarder: fence + copy
     }
     if (!ok) set_abort(bar, a.dev_error);
   } else if (!score && warp == 9) {
@@ -437,17 +553,21 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(DecodeArgs a) {
     for (int j = 0; j < ntiles && ok; ++j) {
       const int st = j % kStages, vs = j % kRecv, os = j % kOwn;
       ok = __all_sync(0xffffffffu, mbar_wait_cluster(&bar.v_full[vs], (j / kRecv) & 1));
+      TR_LAP(7, 0);  // receive warp: waiting for chunks 0-3
       if (!ok) break;
       if (lane == 0) {
         mbar_arrive_expect_tx(&bar.v_full[vs], kHalfBytes);
         mbar_arrive(&bar.s_done[st]);
         mbar_arrive_remote_relaxed(map_peer(smem_u32(&bar.s_done[st]), peer));
       }
+      TR_LAP(7, 1);
       ok = __all_sync(0xffffffffu, mbar_wait(&bar.own_loaded[os], (j / kOwn) & 1));
+      TR_LAP(7, 2);  // receive warp: waiting for own rows
       if (!ok) break;
       fence_proxy_async_smem();  // the own slot's cp.async rows -> PV
       __syncwarp();
       if (lane == 0) mbar_arrive(&bar.p_ok[j % kPSlots]);
+      TR_LAP(7, 3);  // receive warp: fence
     }
     if (!ok) set_abort(bar, a.dev_error);
   } else if (score && warp >= 4 && warp < 10) {
@@ -461,6 +581,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(DecodeArgs a) {
     const uint32_t dS = tbase + kColS + 96 * b + 32 * part;
     bool ok = __all_sync(0xffffffffu, mbar_wait(&bar.q_ready, 0));
     tc_fence_after();
+    TR_LAP(3, 5);
     for (int j = b; ok && j < ntiles; j += kSBuf) {
       const int st = j % kStages, u = j / kSBuf;
       // s_free first: once the softmax has read S(j - 2) it has read every
@@ -468,8 +589,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(DecodeArgs a) {
       // and the kv_full parity below can only mean tile j.  kv_full covers
       // both halves of the tile, this CTA's already fenced into the async
       // proxy by the forwarder.
-      ok = __all_sync(0xffffffffu, mbar_wait(&bar.s_free[b], (u & 1) ^ 1) &&
-                                       mbar_wait_cluster(&bar.kv_full[st], (j / kStages) & 1));
+      ok = __all_sync(0xffffffffu, mbar_wait(&bar.s_free[b], (u & 1) ^ 1));
+      TR_LAP(3, 0);  // S issuer: waiting for the softmax to read the slot
+      ok = ok && __all_sync(0xffffffffu, mbar_wait_cluster(&bar.kv_full[st], (j / kStages) & 1));
+      TR_LAP(3, 1);  // S issuer: waiting for the tile
       if (!ok) break;
       // rows that were not loaded are zero and only reach S columns the
       // softmax masks.  Part 0's arrival passes on (release after the
@@ -488,6 +611,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(DecodeArgs a) {
         mma_commit_mc(&bar.s_done[st], 0x3);
       }
       __syncwarp();
+      TR_LAP(3, 2);  // S issuer: issuing
     }
     if (!ok) set_abort(bar, a.dev_error);
     if (lane == 0) mma_commit(&bar.fin[1 + kSParts * b + part]);
@@ -521,16 +645,23 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(DecodeArgs a) {
     for (int j = sg; ok && j < ntiles; j += 2) {
       const int b = j % kSBuf, slot = j % kPSlots;
       // the other group's m after tile k, read early so that the load's
-      // latency overlaps the wait for S.  Slot k % 8 is posted again at tile
-      // k + 8, which needs PV(j) (through the P slots), so not before this read.
+      // latency overlaps the wait for S.  The read is acknowledged on
+      // m_read (except the first of the two reads of tile 0's max, at tile
+      // 1), and slot k % 8 takes tile k + 8's max only after that.
       float m_other = -INFINITY;
       const int k = j == 1 ? 0 : j - 3;
       if (k >= 0) {
         ok = __all_sync(0xffffffffu, mbar_wait(&bar.m_pub[k & 7], (k >> 3) & 1));
         if (!ok) break;
         m_other = *reinterpret_cast<volatile float*>(&m_ring[(k & 7) * 128 + h]);
+        if (j != 1) {
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&bar.m_read[k & 7]);
+        }
       }
+      TR_LAP(4, 0);  // softmax: the other group's max
       ok = __all_sync(0xffffffffu, mbar_wait(&bar.s_full[b], (j / kSBuf) & 1));
+      TR_LAP(4, 1);  // softmax: waiting for S
       if (!ok) break;
       tc_fence_after();
       const uint32_t mask = *reinterpret_cast<volatile uint32_t*>(&bar.mask[j & 15]);
@@ -549,6 +680,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(DecodeArgs a) {
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bar.s_free[b]);
+      TR_LAP(4, 2);  // softmax: reading S
 #pragma unroll
       for (int i = 0; i < 16; ++i)
         f2_unpack(f2_add(f2_pack(sc[2 * i], sc[2 * i + 1]),
@@ -582,6 +714,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(DecodeArgs a) {
         if (m_used != -INFINITY) l_sum *= ex2_approx(m_used - tmax);
         m_used = tmax;
       }
+      if (j >= 8) {  // the other group has read tile j - 8's max from this slot
+        ok = __all_sync(0xffffffffu, mbar_wait(&bar.m_read[j & 7], ((j - 8) >> 3) & 1));
+        if (!ok) break;
+      }
       m_ring[(j & 7) * 128 + h] = m_used;
       __syncwarp();
       if (lane == 0) mbar_arrive(&bar.m_pub[j & 7]);
@@ -605,7 +741,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(DecodeArgs a) {
       f2_unpack(ps[1], q2, q3);
       l_sum += (q0 + q1) + (q2 + q3);
       // the slot (and this CTA's staging copy of it) is free once PV(j - kPSlots) is done
+      TR_LAP(4, 3);  // softmax: arithmetic
       ok = __all_sync(0xffffffffu, mbar_wait_cluster(&bar.p_free[slot], ((j / kPSlots) & 1) ^ 1));
+      TR_LAP(4, 4);  // softmax: waiting for a free P slot
       if (!ok) break;
       unsigned char* stg = smem + kOffP + slot * kPSlotBytes;
 #pragma unroll
@@ -622,6 +760,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(DecodeArgs a) {
         bulk_copy_to_peer(peer_slot + q4 * kPWarpBytes, stg + q4 * kPWarpBytes, kPWarpBytes, peer_full);
         bulk_copy_to_peer(peer_slot + kPBytes + q4 * 128, stg + kPBytes + q4 * 128, 128, peer_full);
       }
+      TR_LAP(4, 5);  // softmax: P out
     }
     // both groups' normalisers meet here; group 0 finishes the unit
     fin_sh[(2 * sg) * 128 + h] = l_sum;
@@ -670,6 +809,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(DecodeArgs a) {
     for (int j = 0; j < ntiles; ++j) {
       const int vs = j % kRecv, os = j % kOwn, slot = j % kPSlots;
       ok = __all_sync(0xffffffffu, mbar_wait(&bar.p_ok[slot], (j / kPSlots) & 1));
+      TR_LAP(8, 0);  // PV issuer: waiting for p_ok
       if (!ok) break;
       tc_fence_after();
       if (lane == 0) {
@@ -689,6 +829,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(DecodeArgs a) {
         if (j == ntiles - 1) mma_commit(&bar.o_final);
       }
       __syncwarp();
+      TR_LAP(8, 1);  // PV issuer: issuing
     }
     if (!ok) set_abort(bar, a.dev_error);
     if (lane == 0) mma_commit(&bar.fin[0]);
@@ -705,6 +846,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(DecodeArgs a) {
       for (int j = 0; j < ntiles; ++j) {
         const int slot = j % kPSlots;
         ok = __all_sync(0xffffffffu, mbar_wait_cluster(&bar.p_full[slot], (j / kPSlots) & 1));
+        TR_LAP(9, 0);  // value warps 0-3: waiting for P
         if (!ok) break;
         // the slot's next fill (tile j + kPSlots) cannot start before PV(j)
         // frees it, and PV(j) waits for this warp's p_ok below
@@ -736,6 +878,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(DecodeArgs a) {
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&bar.p_ok[slot]);
+        TR_LAP(9, 1);  // value warps 0-3: max check / rescale
       }
     }
     // ------------------------------------------------------------ epilogue
@@ -743,7 +886,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(DecodeArgs a) {
     // 32-column block of a warp's 32 rows goes through a padded shared-memory
     // transpose (stage 0 is idle by now), so that every store instruction
     // writes 128 contiguous bytes of one O row.
+    TR_MARK(9);
     if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&bar.o_final, 0) && mbar_wait_cluster(&bar.fin_l, 0));
+    TR_LAP(9, 2);  // epilogue warps: waiting for the last PV
     if (ok) ok = !__any_sync(0xffffffffu, aborted(bar));
     if (!ok) {
       set_abort(bar, a.dev_error);
@@ -780,6 +925,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(DecodeArgs a) {
   }
 
   // ------------------------------------------------------------- teardown
+  TR_LAP(9, 3);  // epilogue (value warps 0-7), end of role for the others
+  TR_DUMP();
   // the grid that consumes O_part / lse_part may start launching now; it
   // waits for this grid's completion before reading them
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -799,6 +946,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(DecodeArgs a) {
     tc_fence_after();
     tmem_dealloc(tbase, kTmemCols);
   }
+  TR_EXIT(unit);
 }
 
 // Launch order of the units (see launch_unit_order): one CTA; keys count
@@ -914,6 +1062,19 @@ bool decode_tc_supported(const DecodeArgs& a) {
   return a.H <= 128 && (a.plan.chunk % kTile) == 0 &&
          static_cast<int64_t>(a.num_blocks) * a.block_size <= 0x7fffffffLL;
 }
+
+#ifdef DCP_TRACE
+// Traced builds only: copy the counters and the per-CTA timeline of the last
+// launch to the host.
+extern "C" int dcp_trace_fetch(void* dst, size_t bytes) {
+  if (bytes > sizeof(g_dcp_trace)) bytes = sizeof(g_dcp_trace);
+  return static_cast<int>(cudaMemcpyFromSymbol(dst, g_dcp_trace, bytes));
+}
+extern "C" int dcp_timeline_fetch(void* dst, size_t bytes) {
+  if (bytes > sizeof(g_dcp_timeline)) bytes = sizeof(g_dcp_timeline);
+  return static_cast<int>(cudaMemcpyFromSymbol(dst, g_dcp_timeline, bytes));
+}
+#endif
 
 cudaError_t launch_decode_tc(const DecodeArgs& a, cudaStream_t st) {
   if (!decode_tc_supported(a)) return cudaErrorInvalidValue;
