@@ -2,17 +2,25 @@
 // partials (no tensor cores; HBM/L2-bound, and latency-bound when there are
 // few (row, head) pairs).
 //
-// One 128-thread CTA owns one (row, head) pair.  Warp 0 reads the nsrc LSEs
-// (lane d: source d), takes the live set E = {d : lse_d != -inf} as a warp
-// ballot, and publishes the weights exp2(lse_d log2 e - M) (M = max over E;
-// 0 outside E) to shared memory; the partial output of a masked source is
-// never loaded ["[Kimi-K3] DCP support" summary on prhub.com.cn,
-// implementation step 4: -inf at the source, zero-weight sources skipped by
-// the consumer].  Thread t then owns output columns 4t .. 4t+3 and issues
-// the 16-byte loads of up to 8 sources at once, so a pair costs one or two
-// memory round trips instead of one per source.  The kernel waits on the
-// grid it depends on (programmatic dependent launch) only after its launch,
-// so its launch overlaps the tail of the kernel that produced its inputs.
+// kQ warps own one (row, head) pair, each a 512 / kQ-column share of its
+// output, 8 / kQ pairs per CTA.  Lane d of each warp reads source d's LSE,
+// the live set E = {d : lse_d != -inf} is a warp ballot, and the weights
+// exp2(lse_d log2 e - M) (M = max over E) are warp reductions; the partial
+// output of a masked source is never loaded ["[Kimi-K3] DCP support" summary
+// on prhub.com.cn, implementation step 4: -inf at the source, zero-weight
+// sources skipped by the consumer].  Lane t owns kF = 4 / kQ float4 columns
+// of each source (columns 4t + 128k of its warp's share), so every load and
+// store of a warp is a contiguous 512-byte access.
+//   combine (row mask): kQ = 1, one warp per pair, so many pairs per SM keep
+//     enough bytes in flight; the loads of kBatch live sources go out at once.
+//   split merge: kQ = 4, one float4 per source per lane, and since every
+//     split partial is finite (zeros and LSE -inf when its split held no
+//     token) the loads of up to 16 sources start before the weights are
+//     known: one memory round trip.
+// Sources are summed in increasing index order, so results are
+// deterministic.  The kernel waits on the grid it depends on (programmatic
+// dependent launch) only after its launch, so its launch overlaps the tail of
+// the kernel that produced its inputs.
 #include "dcp_kernels.h"
 
 #include <cmath>
@@ -20,9 +28,7 @@
 namespace dcp {
 namespace {
 
-constexpr int kThreadsPerPair = kLatent / 4;  // one float4 column each
-constexpr int kBatch = 8;                     // sources loaded per round trip
-constexpr int kAllAtOnce = 16;                // split merge: sources loaded before the weights are known
+constexpr int kThreads = 256;
 constexpr unsigned kFull = 0xffffffffu;
 
 __device__ __forceinline__ float warp_max(float v) {
@@ -46,112 +52,141 @@ __device__ __forceinline__ void store4(__nv_bfloat16* p, float4 v) {
   *reinterpret_cast<uint2*>(p) = u;
 }
 
-template <typename OutT, bool kRowMask>
-__global__ void __launch_bounds__(kThreadsPerPair)
+__device__ __forceinline__ void fma4(float4& acc, float w, const float4& v) {
+  acc.x = fmaf(w, v.x, acc.x);
+  acc.y = fmaf(w, v.y, acc.y);
+  acc.z = fmaf(w, v.z, acc.z);
+  acc.w = fmaf(w, v.w, acc.w);
+}
+
+template <typename OutT, bool kRowMask, int kBatch>
+__global__ void __launch_bounds__(kThreads)
 lse_merge_kernel(const float* __restrict__ O_src, const float* __restrict__ lse_src,
                  int64_t o_stride, int64_t lse_stride, int nsrc, int64_t npairs, int32_t H,
                  const int32_t* __restrict__ seq_lens, const int32_t* __restrict__ qsl, int32_t B,
                  OutT* __restrict__ out, float* out_lse) {
-  __shared__ float w_s[32];
-  __shared__ float wd_s[32];  // weight by source index (0 if masked)
-  __shared__ int32_t live_s[32];
-  __shared__ int32_t nlive_s;
-  __shared__ float inv_s;
+  constexpr int kQ = kRowMask ? 1 : 4;          // warps per pair
+  constexpr int kF = 4 / kQ;                     // float4 columns per lane per source
+  constexpr int kPairs = kThreads / 32 / kQ;     // pairs per CTA
+  constexpr bool kEarly = !kRowMask;
+  constexpr int kAllAtOnce = 16;                 // split merge: sources loaded before the weights
   asm volatile("griddepcontrol.wait;" ::: "memory");  // inputs written by the preceding grid
-  const int t = threadIdx.x, lane = t & 31;
-  const int64_t pair = blockIdx.x;
-  OutT* dst = out + pair * kLatent + 4 * t;
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  const int64_t pair = static_cast<int64_t>(blockIdx.x) * kPairs + w / kQ;
+  const int share = w % kQ;
+  const bool has = pair < npairs;
+  const float* src = O_src + pair * kLatent + share * (kLatent / kQ) + 4 * lane;
 
-  // Split merge (no row mask): every source is a split partial that the
-  // decode wrote, finite even when its split held no token (zeros, LSE
-  // -inf).  So the partials can be loaded while the weights are still being
-  // worked out: one memory round trip instead of two or three.
-  float4 v_all[kAllAtOnce];
-  const bool all_at_once = !kRowMask && nsrc <= kAllAtOnce;
-  if (all_at_once) {
+  float4 pre[kEarly ? kAllAtOnce : 1];
+  const bool early = kEarly && nsrc <= kAllAtOnce;
+  if (early && has) {
 #pragma unroll
     for (int k = 0; k < kAllAtOnce; ++k)
-      if (k < nsrc) v_all[k] = __ldcs(reinterpret_cast<const float4*>(O_src + k * o_stride + pair * kLatent) + t);
+      if (k < nsrc) pre[k] = __ldcs(reinterpret_cast<const float4*>(src + k * o_stride));
   }
 
-  if (t < 32) {
-    bool pad = false;
-    if (kRowMask) pad = row_is_padding(seq_lens, qsl, B, static_cast<int32_t>(pair / H));
-    // out_lse may alias lse_src's source-0 slice: every read of this pair's
-    // LSEs happens here, before the single write below.
-    const float l = !pad && lane < nsrc ? __ldg(lse_src + lane * lse_stride + pair) : -INFINITY;
-    const bool live = l != -INFINITY;
-    const unsigned live_mask = __ballot_sync(kFull, live);
-    const float l2 = live ? l * kLog2e : -INFINITY;
-    const float M = live_mask ? warp_max(l2) : 0.f;
-    const float w = live ? exp2f(l2 - M) : 0.f;
-    const float den = warp_sum(w);
-    if (live) {
-      const int k = __popc(live_mask & ((1u << lane) - 1u));  // rank among the live sources
-      live_s[k] = lane;
-      w_s[k] = w;
-    }
-    wd_s[lane] = w;
-    if (lane == 0) {
-      nlive_s = __popc(live_mask);
-      inv_s = live_mask ? 1.f / den : 0.f;
-      out_lse[pair] = live_mask ? (M + log2f(den)) * kLn2 : -INFINITY;
-    }
-  }
-  __syncthreads();
-  const int n = nlive_s;
-  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  if (all_at_once) {
-    // sources in increasing index, as below; a masked one adds 0 * finite
+  // the LSE loads go out together with the row's padding test (a padding
+  // row's LSEs are read but ignored)
+  const float l_raw = has && lane < nsrc ? __ldg(lse_src + lane * lse_stride + pair) : -INFINITY;
+  bool pad = false;
+  if (kRowMask && has) pad = row_is_padding(seq_lens, qsl, B, static_cast<int32_t>(pair / H));
+  const float l = pad ? -INFINITY : l_raw;
+  const bool live = l != -INFINITY;
+  const unsigned live_mask = __ballot_sync(kFull, live);
+  const float l2 = live ? l * kLog2e : -INFINITY;
+  const float M = live_mask ? warp_max(l2) : 0.f;
+  const float wt = live ? exp2f(l2 - M) : 0.f;
+  const float den = warp_sum(wt);
+  // out_lse may alias lse_src's source-0 slice: every warp of a pair has read
+  // its LSEs before the single write below (with one warp per pair, the
+  // ballot above already orders them: l_raw is consumed before it)
+  if (kQ > 1) __syncthreads();
+  if (!has) return;
+  if (share == 0 && lane == 0) out_lse[pair] = live_mask ? (M + log2f(den)) * kLn2 : -INFINITY;
+
+  float4 acc[kF];
+#pragma unroll
+  for (int f = 0; f < kF; ++f) acc[f] = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (early) {
+    // in increasing source index; a masked source adds 0 * finite
 #pragma unroll
     for (int k = 0; k < kAllAtOnce; ++k)
-      if (k < nsrc) {
-        const float wd = wd_s[k];
-        acc.x = fmaf(wd, v_all[k].x, acc.x);
-        acc.y = fmaf(wd, v_all[k].y, acc.y);
-        acc.z = fmaf(wd, v_all[k].z, acc.z);
-        acc.w = fmaf(wd, v_all[k].w, acc.w);
-      }
-  }
-  for (int k0 = 0; !all_at_once && k0 < n; k0 += kBatch) {
-    float4 v[kBatch];
+      if (k < nsrc) fma4(acc[0], __shfl_sync(kFull, wt, k), pre[k]);
+  } else {
+    unsigned m = live_mask;  // padding row or no live source: m == 0, so zeros
+    while (m) {
+      int ds[kBatch];
+      int n = 0;
 #pragma unroll
-    for (int k = 0; k < kBatch; ++k)
-      if (k0 + k < n)
-        v[k] = __ldcs(reinterpret_cast<const float4*>(O_src + live_s[k0 + k] * o_stride + pair * kLatent) + t);
-#pragma unroll
-    for (int k = 0; k < kBatch; ++k)
-      if (k0 + k < n) {
-        const float wd = w_s[k0 + k];
-        acc.x = fmaf(wd, v[k].x, acc.x);
-        acc.y = fmaf(wd, v[k].y, acc.y);
-        acc.z = fmaf(wd, v[k].z, acc.z);
-        acc.w = fmaf(wd, v[k].w, acc.w);
+      for (int i = 0; i < kBatch; ++i) {
+        ds[i] = m ? __ffs(m) - 1 : 0;
+        n += m ? 1 : 0;
+        m &= m - 1;
       }
+      float4 v[kBatch][kF];
+#pragma unroll
+      for (int i = 0; i < kBatch; ++i)
+        if (i < n) {
+#pragma unroll
+          for (int f = 0; f < kF; ++f) v[i][f] = __ldcs(reinterpret_cast<const float4*>(src + ds[i] * o_stride + 128 * f));
+        }
+#pragma unroll
+      for (int i = 0; i < kBatch; ++i)
+        if (i < n) {
+          const float wd = __shfl_sync(kFull, wt, ds[i]);
+#pragma unroll
+          for (int f = 0; f < kF; ++f) fma4(acc[f], wd, v[i][f]);
+        }
+    }
   }
-  // padding row or no live source: n == 0, inv == 0, so zeros
-  const float inv = inv_s;
-  acc.x *= inv; acc.y *= inv; acc.z *= inv; acc.w *= inv;
-  store4(dst, acc);
+  const float inv = live_mask ? 1.f / den : 0.f;
+  OutT* dst = out + pair * kLatent + share * (kLatent / kQ) + 4 * lane;
+#pragma unroll
+  for (int f = 0; f < kF; ++f)
+    store4(dst + 128 * f, make_float4(acc[f].x * inv, acc[f].y * inv, acc[f].z * inv, acc[f].w * inv));
 }
 
-template <typename OutT, bool kRowMask>
-cudaError_t launch(const float* O_src, const float* lse_src, int64_t o_stride, int64_t lse_stride,
-                   int nsrc, int64_t npairs, int32_t H, const int32_t* seq_lens, const int32_t* qsl,
-                   int32_t B, OutT* out, float* out_lse, cudaStream_t st) {
-  if (npairs <= 0) return cudaSuccess;
-  if (npairs > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+template <bool kRowMask>
+constexpr int pairs_per_cta() { return kThreads / 32 / (kRowMask ? 1 : 4); }
+
+template <typename OutT, bool kRowMask, int kBatch>
+cudaError_t launch_batch(const float* O_src, const float* lse_src, int64_t o_stride, int64_t lse_stride,
+                         int nsrc, int64_t npairs, int32_t H, const int32_t* seq_lens, const int32_t* qsl,
+                         int32_t B, OutT* out, float* out_lse, cudaStream_t st) {
+  const int64_t ctas = (npairs + pairs_per_cta<kRowMask>() - 1) / pairs_per_cta<kRowMask>();
+  if (ctas > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(npairs));
-  cfg.blockDim = dim3(kThreadsPerPair);
+  cfg.gridDim = dim3(static_cast<unsigned>(ctas));
+  cfg.blockDim = dim3(kThreads);
   cfg.stream = st;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, lse_merge_kernel<OutT, kRowMask>, O_src, lse_src, o_stride, lse_stride, nsrc,
-                            npairs, H, seq_lens, qsl, B, out, out_lse);
+  return cudaLaunchKernelEx(&cfg, lse_merge_kernel<OutT, kRowMask, kBatch>, O_src, lse_src, o_stride, lse_stride,
+                            nsrc, npairs, H, seq_lens, qsl, B, out, out_lse);
+}
+
+// The combine (one warp per pair, four float4 columns per lane per source)
+// loads two live sources at a time when there are at most two, else four:
+// fewer registers for small D leave room for more pairs per SM.  The split
+// merge (one float4 per lane per source) loads up to 16 at a time.
+template <typename OutT, bool kRowMask>
+cudaError_t launch(const float* O_src, const float* lse_src, int64_t o_stride, int64_t lse_stride,
+                   int nsrc, int64_t npairs, int32_t H, const int32_t* seq_lens, const int32_t* qsl,
+                   int32_t B, OutT* out, float* out_lse, cudaStream_t st) {
+  if (npairs <= 0) return cudaSuccess;
+  if constexpr (!kRowMask) {
+    return launch_batch<OutT, kRowMask, 16>(O_src, lse_src, o_stride, lse_stride, nsrc, npairs, H, seq_lens, qsl, B,
+                                            out, out_lse, st);
+  } else {
+    if (nsrc <= 2)
+      return launch_batch<OutT, kRowMask, 2>(O_src, lse_src, o_stride, lse_stride, nsrc, npairs, H, seq_lens, qsl, B,
+                                             out, out_lse, st);
+    return launch_batch<OutT, kRowMask, 4>(O_src, lse_src, o_stride, lse_stride, nsrc, npairs, H, seq_lens, qsl, B,
+                                           out, out_lse, st);
+  }
 }
 
 }  // namespace

@@ -40,16 +40,40 @@ DCP_HD int64_t local_to_global(int64_t j, int32_t d, int32_t D, int32_t I) {
   return (j / I) * (static_cast<int64_t>(D) * I) + static_cast<int64_t>(d) * I + j % I;
 }
 
-// Request owning query row r: the b with qsl[b] <= r < qsl[b+1], or -1 when
-// r lies before qsl[0] or at/after qsl[B].  qsl is non-decreasing.
-__device__ __forceinline__ int32_t find_request(const int32_t* __restrict__ qsl, int32_t B, int32_t r) {
-  if (B <= 0 || r < __ldg(qsl) || r >= __ldg(qsl + B)) return -1;
+// The request owning query row r, with its row range and seq_len: b is the
+// request with qsl[b] <= r < qsl[b+1] (unique: qsl is non-decreasing), or -1
+// when r lies before qsl[0] or at/after qsl[B].  Batches whose requests all
+// have the same number of rows (one decode row each, or a fixed verification
+// width) resolve in two rounds of independent loads: the guess
+// g = (r - qsl[0]) / (qsl[1] - qsl[0]) is checked against qsl[g], qsl[g+1]
+// (loaded together with seq_lens[g]); any other layout falls back to a
+// binary search.
+struct RequestOfRow {
+  int32_t b;       // -1 if none
+  int32_t q0, q1;  // qsl[b], qsl[b+1]
+  int32_t seq;     // seq_lens[b]
+};
+
+__device__ __forceinline__ RequestOfRow request_of_row(const int32_t* __restrict__ seq_lens,
+                                                       const int32_t* __restrict__ qsl, int32_t B, int32_t r) {
+  RequestOfRow q{-1, 0, 0, 0};
+  if (B <= 0) return q;
+  const int32_t qa = __ldg(qsl), qn = __ldg(qsl + 1), qB = __ldg(qsl + B);
+  if (r < qa || r >= qB) return q;
+  const int32_t step = qn - qa;
+  if (step > 0) {
+    const int32_t g = (r - qa) / step;
+    if (g < B) {
+      const int32_t lo = __ldg(qsl + g), hi = __ldg(qsl + g + 1), sq = __ldg(seq_lens + g);
+      if (lo <= r && r < hi) return RequestOfRow{g, lo, hi, sq};
+    }
+  }
   int32_t lo = 0, hi = B;  // invariant: qsl[lo] <= r < qsl[hi]
   while (hi - lo > 1) {
     const int32_t mid = (lo + hi) >> 1;
     if (__ldg(qsl + mid) <= r) lo = mid; else hi = mid;
   }
-  return lo;
+  return RequestOfRow{lo, __ldg(qsl + lo), __ldg(qsl + lo + 1), __ldg(seq_lens + lo)};
 }
 
 struct RowInfo {
@@ -67,16 +91,15 @@ __device__ __forceinline__ RowInfo resolve_row(const int32_t* __restrict__ seq_l
                                                const int32_t* __restrict__ qsl, int32_t B,
                                                int32_t r, int32_t max_seq_len, int32_t max_q_len) {
   RowInfo ri{-1, 0, true, 0u};
-  const int32_t b = find_request(qsl, B, r);
-  if (b < 0) return ri;
-  ri.b = b;
-  int32_t seq = __ldg(seq_lens + b);
+  const RequestOfRow q = request_of_row(seq_lens, qsl, B, r);
+  if (q.b < 0) return ri;
+  ri.b = q.b;
+  int32_t seq = q.seq;
   if (seq <= 0) return ri;  // CUDA-graph padding request (negative: treated alike)
-  const int32_t q0 = __ldg(qsl + b), q1 = __ldg(qsl + b + 1);
-  const int32_t q_len = q1 - q0;
+  const int32_t q_len = q.q1 - q.q0;
   if (q_len > max_q_len) ri.err |= DCP_DEVERR_BAD_ROWS;
   if (seq > max_seq_len) { ri.err |= DCP_DEVERR_SEQ_TOO_LONG; seq = max_seq_len; }
-  const int32_t L = seq - (q_len - 1 - (r - q0));
+  const int32_t L = seq - (q_len - 1 - (r - q.q0));
   ri.L = L > 0 ? L : 0;
   ri.padding = false;
   return ri;
@@ -87,8 +110,8 @@ __device__ __forceinline__ RowInfo resolve_row(const int32_t* __restrict__ seq_l
 // follow-up and the review thread on the seq_lens == 0 row mask).
 __device__ __forceinline__ bool row_is_padding(const int32_t* __restrict__ seq_lens,
                                                const int32_t* __restrict__ qsl, int32_t B, int32_t r) {
-  const int32_t b = find_request(qsl, B, r);
-  return b < 0 || __ldg(seq_lens + b) <= 0;
+  const RequestOfRow q = request_of_row(seq_lens, qsl, B, r);
+  return q.b < 0 || q.seq <= 0;
 }
 
 // Split-KV plan shared by the workspace query and the launch: each (row,
