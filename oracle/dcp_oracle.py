@@ -17,7 +17,9 @@ It states, as plainly as possible, what the hot path computes:
    a shard with no tokens, or a padding row, gets L_d = -inf and O_d = NaN
    (NaN on purpose: a correct combine never reads it);
 5. the LSE-weighted combine over shards with empty-shard and padding-row
-   masking.
+   masking;
+6. the step before attention: the decode query ``[ql_nope | q_pe]`` and the
+   write of this step's latent rows into the paged cache.
 
 Sources (pages on decode context parallelism for MLA):
   [PR50484]  "[Kimi-K3] DCP support", vllm-project/vllm pull request 50484
@@ -48,7 +50,7 @@ KDIM = LATENT + ROPE  # 576: query head row = [q absorbed into latent | q_pe]
 __all__ = [
     "bf16_to_f64", "row_lengths", "shard_of", "local_len", "shard_positions",
     "physical_rows", "gather_latents", "scores", "shard_partial",
-    "decode_partial_row", "decode_partial", "lse_combine", "attention",
+    "decode_partial_row", "decode_partial", "lse_combine", "attention", "concat_cache",
 ]
 
 
@@ -257,3 +259,39 @@ def attention(q_heads_f64: np.ndarray, latents: np.ndarray, scale: float):
     Returns (out [H, 512], lse [H]); latents [L, 576] float64, L > 0."""
     s = scores(q_heads_f64, latents, scale)
     return shard_partial(s, latents[:, :LATENT])
+
+
+# ---------------------------------------------------------------------------
+# the step before attention: query concat and paged-cache write
+# ---------------------------------------------------------------------------
+def concat_cache(ql_nope: np.ndarray, q_pe: np.ndarray, kv_c: np.ndarray, k_pe: np.ndarray,
+                 slot_mapping: np.ndarray, kv_cache: np.ndarray):
+    """The fused decode step that precedes ``forward_mqa`` [PRHUB, snippet
+    "Decode: latent multi-query attention": ``_decode_concat_cache`` builds
+    the query ``[ql_nope | q_pe]`` and writes this step's ``kv_c_normed`` and
+    ``k_pe`` into the paged cache at ``slot_mapping``, in one launch; the
+    optional RoPE positions are None].
+
+    Inputs are bf16 bit patterns (uint16): ql_nope [T, H, 512], q_pe
+    [T, H, 64], kv_c [T, 512], k_pe [T, 64]; slot_mapping int [T] holds each
+    token's cache row (block * block_size + offset), a negative value meaning
+    "not written here" (a padding token, or a token another DCP rank owns);
+    kv_cache [num_blocks, block_size, 576].  Returns (q [T, H, 576], the new
+    cache): a byte copy, so bit-exact.
+    """
+    ql_nope = np.asarray(ql_nope, dtype=np.uint16)
+    q_pe = np.asarray(q_pe, dtype=np.uint16)
+    T, H = ql_nope.shape[:2]
+    q = np.empty((T, H, KDIM), dtype=np.uint16)
+    q[:, :, :LATENT] = ql_nope
+    q[:, :, LATENT:] = q_pe
+    cache = np.array(kv_cache, dtype=np.uint16, copy=True)
+    nb, bs, _ = cache.shape
+    flat = cache.reshape(nb * bs, KDIM)
+    for t in range(T):
+        slot = int(slot_mapping[t])
+        if slot < 0:
+            continue
+        flat[slot, :LATENT] = kv_c[t]
+        flat[slot, LATENT:] = k_pe[t]
+    return q, cache

@@ -290,3 +290,53 @@ def check_combine_permutation(o):
         out, ol = o.lse_combine(O[p], l[p], pad)
         assert np.allclose(out, base, rtol=1e-12, atol=1e-12)
         assert np.allclose(ol, bl, rtol=1e-12, atol=1e-12)
+
+
+# ---------------------------------------------------------------------------
+# the step before attention: query concat + paged-cache write
+# ---------------------------------------------------------------------------
+def concat_cache_case(seed: int = 7, T: int = 6, H: int = 3, nb: int = 5, bs: int = 4):
+    """Small random bf16 inputs for concat_cache: slots include a padding
+    token (-1) and tokens scattered over permuted blocks."""
+    rng = np.random.default_rng(seed)
+    bits = lambda *shape: rng.integers(0, 1 << 16, size=shape, dtype=np.uint16)
+    slots = rng.choice(nb * bs, size=T, replace=False).astype(np.int64)
+    slots[1] = -1
+    return dict(ql_nope=bits(T, H, 512), q_pe=bits(T, H, 64), kv_c=bits(T, 512), k_pe=bits(T, 64),
+                slot_mapping=slots, kv_cache=bits(nb, bs, 576))
+
+
+def check_concat_cache(o):
+    """The query is torch.cat of the two parts; the cache equals the old cache
+    with exactly the rows of non-negative slots replaced by torch.cat of the
+    latent and rope parts (torch index_copy_), every other byte unchanged."""
+    c = concat_cache_case()
+    q, cache = o.concat_cache(c["ql_nope"], c["q_pe"], c["kv_c"], c["k_pe"], c["slot_mapping"], c["kv_cache"])
+    tq = lambda a: torch.from_numpy(np.asarray(a).astype(np.int32))
+    want_q = torch.cat([tq(c["ql_nope"]), tq(c["q_pe"])], dim=-1).numpy().astype(np.uint16)
+    assert q.shape == want_q.shape and np.array_equal(q, want_q)
+    nb, bs, _ = c["kv_cache"].shape
+    keep = c["slot_mapping"] >= 0
+    idx = torch.from_numpy(c["slot_mapping"][keep])
+    rows = torch.cat([tq(c["kv_c"]), tq(c["k_pe"])], dim=-1)[torch.from_numpy(keep)]
+    want = tq(c["kv_cache"]).reshape(nb * bs, 576).index_copy_(0, idx, rows)
+    assert np.array_equal(cache.reshape(nb * bs, 576), want.numpy().astype(np.uint16))
+    # the input cache is not modified in place
+    assert not np.shares_memory(cache, c["kv_cache"])
+
+
+def check_concat_cache_feeds_the_walker(o):
+    """A token written at the slot of logical position p of a request (its
+    block-table entry) is what the block-table walker reads back at p."""
+    rng = np.random.default_rng(11)
+    nb, bs, L = 6, 4, 13
+    table = rng.permutation(nb).astype(np.int64)
+    cache = np.zeros((nb, bs, 576), dtype=np.uint16)
+    kv_c = rng.integers(0, 0x7000, size=(1, 512), dtype=np.uint16)  # finite bf16 patterns
+    k_pe = rng.integers(0, 0x7000, size=(1, 64), dtype=np.uint16)
+    slot = np.array([table[L // bs] * bs + L % bs])
+    _, cache = o.concat_cache(np.zeros((1, 1, 512), np.uint16), np.zeros((1, 1, 64), np.uint16), kv_c, k_pe,
+                              slot, cache)
+    got = o.gather_latents(cache, table, bs, np.array([L]))
+    want = o.bf16_to_f64(np.concatenate([kv_c, k_pe], axis=-1))
+    assert np.array_equal(got, want)

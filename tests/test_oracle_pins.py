@@ -92,3 +92,11 @@ def test_generator_is_deterministic_and_poisoned():
     t = a["block_table"]
     assert (t[0, 1:] == -1).all()
     assert a["kv_cache"].reshape(-1, 576)[t[0, 0] * 16 + 1, 0] == wl.BF16_NAN
+
+
+def test_concat_cache_is_cat_and_scatter():
+    C.check_concat_cache(oracle)
+
+
+def test_concat_cache_feeds_the_walker():
+    C.check_concat_cache_feeds_the_walker(oracle)

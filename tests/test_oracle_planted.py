@@ -90,3 +90,36 @@ def test_values_from_wrong_dims_are_caught(monkeypatch):
     monkeypatch.setattr(O, "shard_partial", lambda s, v: real(s, np.roll(v, 64, axis=1)))
     inp = wl.make_decode_inputs(wl.TINY)
     _fails(C.check_decode_rows_vs_torch, inp)
+
+
+def _concat_variant(swap=False, neg_wraps=False, drop_pe=False):
+    def f(ql_nope, q_pe, kv_c, k_pe, slot_mapping, kv_cache):
+        T, H = ql_nope.shape[:2]
+        q = np.empty((T, H, 576), dtype=np.uint16)
+        q[:, :, :512] = ql_nope
+        q[:, :, 512:] = 0 if drop_pe else q_pe
+        cache = np.array(kv_cache, copy=True)
+        flat = cache.reshape(-1, 576)
+        for t in range(T):
+            s = int(slot_mapping[t])
+            if s < 0 and not neg_wraps:
+                continue
+            row = np.concatenate([k_pe[t], kv_c[t]]) if swap else np.concatenate([kv_c[t], k_pe[t]])
+            flat[s] = row
+        return q, cache
+    return f
+
+
+def test_concat_cache_rope_first_is_caught(monkeypatch):
+    monkeypatch.setattr(O, "concat_cache", _concat_variant(swap=True))
+    _fails(C.check_concat_cache)
+
+
+def test_concat_cache_negative_slot_written_is_caught(monkeypatch):
+    monkeypatch.setattr(O, "concat_cache", _concat_variant(neg_wraps=True))
+    _fails(C.check_concat_cache)
+
+
+def test_concat_cache_dropped_q_pe_is_caught(monkeypatch):
+    monkeypatch.setattr(O, "concat_cache", _concat_variant(drop_pe=True))
+    _fails(C.check_concat_cache)
