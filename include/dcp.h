@@ -218,6 +218,51 @@ dcp_status_t dcp_lse_combine(
     void* out, dcp_dtype_t out_dtype, float* out_lse, void* stream);
 
 /*
+ * The decode step before attention, fused into one launch ["[Kimi-K3] DCP
+ * support" summary on prhub.com.cn, key snippet "Decode: latent multi-query
+ * attention": _decode_concat_cache builds the decode query and writes this
+ * step's latent rows into the paged cache before forward_mqa, so the decode
+ * call sees the new tokens (seq_lens count them)].  The optional RoPE of the
+ * snippet (rope_positions = None) is not applied: the rope parts are taken as
+ * given.
+ *
+ * For every token t < T and head h < H:
+ *   q_out[t, h, 0:512]   = ql_nope[t, h, :]
+ *   q_out[t, h, 512:576] = q_pe[t, h, :]
+ * and, when 0 <= slot_mapping[t] < num_slots:
+ *   kv_cache[slot_mapping[t], 0:512]   = kv_c[t, :]
+ *   kv_cache[slot_mapping[t], 512:576] = k_pe[t, :]
+ * slot_mapping[t] = block * block_size + offset is the token's cache row.  A
+ * negative slot is not written: a padding token, or (with per-rank caches) a
+ * token another DCP rank owns.  A slot >= num_slots is not written either and
+ * sets DCP_DEVERR_BAD_BLOCK in *dev_error.  Byte copies: bit-exact.
+ *
+ *   ql_nope      bf16 [T, H, 512]; element (t, h, k) at t * ql_nope_stride_tok +
+ *                h * ql_nope_stride_head + k (e.g. the transposed output of the
+ *                per-head q_nope x W_UK batched matmul).
+ *   q_pe         bf16 [T, H, 64], strides likewise.
+ *   kv_c, k_pe   bf16 [T, 512] and [T, 64], rows kv_c_stride_tok /
+ *                k_pe_stride_tok apart.
+ *   slot_mapping int64 [T], device.
+ *   q_out        bf16 [T, H, 576], heads dense, rows q_out_stride_tok apart
+ *                (>= H * 576); must not overlap any input.
+ *   kv_cache     bf16 [num_slots, 576] (num_blocks * block_size rows); two
+ *                tokens must not share a slot.
+ * Every pointer is 16-byte aligned and every stride a multiple of 8
+ * elements, else DCP_ERR_MISALIGNED.  T == 0 returns DCP_OK without
+ * launching anything.
+ */
+dcp_status_t dcp_decode_concat_cache(
+    const void* ql_nope, int64_t ql_nope_stride_tok, int64_t ql_nope_stride_head,
+    const void* q_pe, int64_t q_pe_stride_tok, int64_t q_pe_stride_head,
+    const void* kv_c, int64_t kv_c_stride_tok,
+    const void* k_pe, int64_t k_pe_stride_tok,
+    const int64_t* slot_mapping, int32_t T, int32_t H,
+    void* q_out, int64_t q_out_stride_tok,
+    void* kv_cache, int64_t num_slots,
+    int32_t* dev_error, void* stream);
+
+/*
  * dcp_mla_decode_partial without a workspace argument, for callers that
  * cannot allocate device memory (their memory is owned and fully reserved by
  * a host framework, or they are plugins handed only their inputs and

@@ -55,6 +55,8 @@ EXPORTS = [
      [_P, _I64, _P, _I32, _I32, _P, _I32, _I64, _P, _P, _I32, _I32, _I32, _I32, _I32, _I32, _I32, _F,
       _P, _P, _P, _SZ, _P, _P]),
     ("dcp_lse_combine", ctypes.c_int, [_P, _P, _P, _P, _I32, _I32, _I32, _I32, _P, ctypes.c_int, _P, _P]),
+    ("dcp_decode_concat_cache", ctypes.c_int,
+     [_P, _I64, _I64, _P, _I64, _I64, _P, _I64, _P, _I64, _P, _I32, _I32, _P, _I64, _P, _I64, _P, _P]),
     ("dcp_mla_decode_partial_noalloc", ctypes.c_int,
      [_P, _I64, _P, _I32, _I32, _P, _I32, _I64, _P, _P, _I32, _I32, _I32, _I32, _I32, _I32, _I32, _F,
       _P, _P, _P, _P]),
@@ -314,6 +316,47 @@ def dcp_lse_combine(O_part, lse_part, seq_lens, query_start_loc, out, out_lse, *
     _check(st, "dcp_lse_combine")
 
 
+def dcp_decode_concat_cache(ql_nope, q_pe, kv_c, k_pe, slot_mapping, q_out, kv_cache, *,
+                            dev_error: Optional[torch.Tensor] = None, stream=None) -> None:
+    """ql_nope bf16 [T, H, 512], q_pe bf16 [T, H, 64] (any token/head strides,
+    unit element stride), kv_c bf16 [T, 512], k_pe bf16 [T, 64] (row strides
+    allowed), slot_mapping int64 [T]; writes q_out bf16 [T, H, 576] and the
+    rows of kv_cache bf16 [num_blocks, block_size, 576] at the non-negative
+    slots."""
+    for name, t, dt, dims, last in (("ql_nope", ql_nope, torch.bfloat16, 3, LATENT_DIM),
+                                    ("q_pe", q_pe, torch.bfloat16, 3, ROPE_DIM),
+                                    ("kv_c", kv_c, torch.bfloat16, 2, LATENT_DIM),
+                                    ("k_pe", k_pe, torch.bfloat16, 2, ROPE_DIM),
+                                    ("q_out", q_out, torch.bfloat16, 3, KV_DIM)):
+        if not isinstance(t, torch.Tensor) or t.dtype != dt:
+            raise TypeError("%s must be a %s tensor" % (name, dt))
+        if t.dim() != dims or t.shape[-1] != last or t.stride(-1) != 1:
+            raise ValueError("%s must have %d dims, last of size %d with unit stride" % (name, dims, last))
+    T, H = ql_nope.shape[0], ql_nope.shape[1]
+    if tuple(q_pe.shape[:2]) != (T, H) or kv_c.shape[0] != T or k_pe.shape[0] != T:
+        raise ValueError("ql_nope, q_pe, kv_c and k_pe disagree on T or H")
+    if tuple(q_out.shape[:2]) != (T, H) or q_out.stride(1) != KV_DIM:
+        raise ValueError("q_out must be [T, H, 576] with dense heads")
+    if not isinstance(slot_mapping, torch.Tensor) or slot_mapping.dtype != torch.int64 or \
+            tuple(slot_mapping.shape) != (T,):
+        raise ValueError("slot_mapping must be an int64 [T] tensor")
+    if not isinstance(kv_cache, torch.Tensor) or kv_cache.dtype != torch.bfloat16 or kv_cache.dim() != 3 or \
+            kv_cache.shape[2] != KV_DIM:
+        raise ValueError("kv_cache must be bf16 [num_blocks, block_size, 576]")
+    for name, t in (("ql_nope", ql_nope), ("q_pe", q_pe), ("kv_c", kv_c), ("k_pe", k_pe), ("q_out", q_out)):
+        _need(t, name, torch.bfloat16, contiguous=False)
+    _need(slot_mapping, "slot_mapping", torch.int64)
+    _need(kv_cache, "kv_cache", torch.bfloat16)
+    _need_opt(dev_error, "dev_error", torch.int32)
+    with _Range("dcp_decode_concat_cache"):
+        st = lib().dcp_decode_concat_cache(
+            _ptr(ql_nope), ql_nope.stride(0), ql_nope.stride(1), _ptr(q_pe), q_pe.stride(0), q_pe.stride(1),
+            _ptr(kv_c), kv_c.stride(0), _ptr(k_pe), k_pe.stride(0), _ptr(slot_mapping), T, H, _ptr(q_out),
+            q_out.stride(0), _ptr(kv_cache), kv_cache.shape[0] * kv_cache.shape[1], _ptr(dev_error),
+            _stream(stream))
+    _check(st, "dcp_decode_concat_cache")
+
+
 # ----------------------------------------------------------------------------
 # allocating conveniences
 # ----------------------------------------------------------------------------
@@ -354,3 +397,13 @@ def lse_combine(O_part, lse_part, seq_lens, query_start_loc, out_dtype=torch.bfl
     out_lse = torch.empty((T, H), dtype=torch.float32, device=O_part.device)
     dcp_lse_combine(O_part, lse_part, seq_lens, query_start_loc, out, out_lse, stream=stream)
     return out, out_lse
+
+
+def decode_concat_cache(ql_nope, q_pe, kv_c, k_pe, slot_mapping, kv_cache, dev_error=None, stream=None):
+    """Allocating form: returns the decode query q bf16 [T, H, 576]; writes
+    the step's latent rows into kv_cache in place."""
+    T, H = ql_nope.shape[0], ql_nope.shape[1]
+    q = torch.empty((T, H, KV_DIM), dtype=torch.bfloat16, device=ql_nope.device)
+    dcp_decode_concat_cache(ql_nope, q_pe, kv_c, k_pe, slot_mapping, q, kv_cache, dev_error=dev_error,
+                            stream=stream)
+    return q

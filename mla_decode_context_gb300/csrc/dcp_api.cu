@@ -271,4 +271,36 @@ dcp_status_t dcp_lse_combine(const float* O_part, const float* lse_part, const i
   return e == cudaSuccess ? DCP_OK : DCP_ERR_CUDA;
 }
 
+dcp_status_t dcp_decode_concat_cache(const void* ql_nope, int64_t ql_nope_stride_tok, int64_t ql_nope_stride_head,
+                                     const void* q_pe, int64_t q_pe_stride_tok, int64_t q_pe_stride_head,
+                                     const void* kv_c, int64_t kv_c_stride_tok, const void* k_pe,
+                                     int64_t k_pe_stride_tok, const int64_t* slot_mapping, int32_t T, int32_t H,
+                                     void* q_out, int64_t q_out_stride_tok, void* kv_cache, int64_t num_slots,
+                                     int32_t* dev_error, void* stream) {
+  if (T < 0 || H < 1 || num_slots < 1) return DCP_ERR_INVALID_ARG;
+  if (T == 0) return DCP_OK;
+  if (!ql_nope || !q_pe || !kv_c || !k_pe || !slot_mapping || !q_out || !kv_cache) return DCP_ERR_INVALID_ARG;
+  if (ql_nope_stride_tok < 0 || ql_nope_stride_head < 0 || q_pe_stride_tok < 0 || q_pe_stride_head < 0 ||
+      kv_c_stride_tok < 0 || k_pe_stride_tok < 0 || q_out_stride_tok < static_cast<int64_t>(H) * DCP_KV_DIM)
+    return DCP_ERR_INVALID_ARG;
+  const int64_t strides[] = {ql_nope_stride_tok, ql_nope_stride_head, q_pe_stride_tok, q_pe_stride_head,
+                             kv_c_stride_tok,    k_pe_stride_tok,     q_out_stride_tok};
+  for (int64_t st : strides)
+    if (st % 8 != 0) return DCP_ERR_MISALIGNED;  // 16-byte units
+  if (!aligned16(ql_nope) || !aligned16(q_pe) || !aligned16(kv_c) || !aligned16(k_pe) || !aligned16(q_out) ||
+      !aligned16(kv_cache))
+    return DCP_ERR_MISALIGNED;
+  dcp::ConcatCacheArgs a{};
+  a.ql_nope = ql_nope; a.ql_nope_stride_tok = ql_nope_stride_tok; a.ql_nope_stride_head = ql_nope_stride_head;
+  a.q_pe = q_pe; a.q_pe_stride_tok = q_pe_stride_tok; a.q_pe_stride_head = q_pe_stride_head;
+  a.kv_c = kv_c; a.kv_c_stride_tok = kv_c_stride_tok;
+  a.k_pe = k_pe; a.k_pe_stride_tok = k_pe_stride_tok;
+  a.slot_mapping = slot_mapping;
+  a.T = T; a.H = H;
+  a.q_out = q_out; a.q_out_stride_tok = q_out_stride_tok;
+  a.kv_cache = kv_cache; a.num_slots = num_slots;
+  a.dev_error = dev_error;
+  return dcp::launch_concat_cache(a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? DCP_OK : DCP_ERR_CUDA;
+}
+
 }  // extern "C"

@@ -53,6 +53,27 @@ cudaError_t launch_lse_merge_f32(const float* O_src, const float* lse_src, int64
 // Reference SIMT decode (fp32 FMA, any geometry).
 cudaError_t launch_decode_simt(const DecodeArgs& a, cudaStream_t st);
 
+// The decode step before attention: query concat and paged-cache write
+// (validated by the C ABI; strides in elements, 16-byte aligned).
+struct ConcatCacheArgs {
+  const void* ql_nope;  // bf16 [T, H, 512]
+  int64_t ql_nope_stride_tok, ql_nope_stride_head;
+  const void* q_pe;     // bf16 [T, H, 64]
+  int64_t q_pe_stride_tok, q_pe_stride_head;
+  const void* kv_c;     // bf16 [T, 512]
+  int64_t kv_c_stride_tok;
+  const void* k_pe;     // bf16 [T, 64]
+  int64_t k_pe_stride_tok;
+  const int64_t* slot_mapping;  // [T]
+  int32_t T, H;
+  void* q_out;          // bf16 [T, H, 576]
+  int64_t q_out_stride_tok;
+  void* kv_cache;       // bf16 [num_slots, 576]
+  int64_t num_slots;
+  int32_t* dev_error;
+};
+cudaError_t launch_concat_cache(const ConcatCacheArgs& a, cudaStream_t st);
+
 // Tensor-core decode (tcgen05/TMEM/TMA, 2-CTA clusters).  Supported when
 // H <= 128 and the shard layout tiles into whole TMA boxes: block_size a
 // multiple of D * interleave (runs inside blocks) or interleave a multiple

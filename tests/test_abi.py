@@ -201,3 +201,22 @@ def test_combine_wrapper_checks_shapes_before_the_device():
         dcp.dcp_lse_combine(O, lse, seq, torch.zeros(2, dtype=torch.int32), out, out_lse)
     with pytest.raises(ValueError, match="CUDA tensor"):
         dcp.dcp_lse_combine(O, lse, seq, qsl, out, out_lse)
+
+
+def _concat(L, **kw):
+    a = dict(qn=0x1000, qn_t=512, qn_h=512, qp=0x2000, qp_t=64, qp_h=64, kc=0x3000, kc_t=512, kp=0x4000, kp_t=64,
+             slot=0x5000, T=2, H=1, qo=0x6000, qo_t=576, cache=0x7000, nslots=16, err=None)
+    a.update(kw)
+    return L.dcp_decode_concat_cache(a["qn"], a["qn_t"], a["qn_h"], a["qp"], a["qp_t"], a["qp_h"], a["kc"], a["kc_t"],
+                                     a["kp"], a["kp_t"], a["slot"], a["T"], a["H"], a["qo"], a["qo_t"], a["cache"],
+                                     a["nslots"], a["err"], None)
+
+
+def test_concat_cache_validation_returns_before_launch(L):
+    assert _concat(L, T=0) == 0
+    assert _concat(L, T=-1) == 1 and _concat(L, H=0) == 1 and _concat(L, nslots=0) == 1
+    assert _concat(L, slot=None) == 1 and _concat(L, qo=None) == 1
+    assert _concat(L, qo_t=575) == 1                  # output rows narrower than H * 576
+    assert _concat(L, qn=0x1008) == 3                 # 16-byte rule
+    assert _concat(L, kc_t=516) == 3                  # strides in whole 16-byte units
+    assert _concat(L, cache=0x7004) == 3
