@@ -49,7 +49,7 @@ KDIM = LATENT + ROPE  # 576: query head row = [q absorbed into latent | q_pe]
 
 __all__ = [
     "bf16_to_f64", "row_lengths", "shard_of", "local_len", "shard_positions",
-    "physical_rows", "gather_latents", "scores", "shard_partial",
+    "physical_rows", "physical_rows_local", "gather_latents", "scores", "shard_partial",
     "decode_partial_row", "decode_partial", "lse_combine", "attention", "concat_cache",
 ]
 
@@ -140,6 +140,19 @@ def physical_rows(table_row: np.ndarray, block_size: int, positions: np.ndarray)
     return blocks * block_size + positions % block_size
 
 
+def physical_rows_local(shard_table_row: np.ndarray, block_size: int, n: int) -> np.ndarray:
+    """Per-shard (DCP rank-local) layout: a shard stores only its own tokens,
+    densely and in order, so its j-th token (the j-th position it owns) lives
+    in row table[j // block_size] * block_size + j % block_size of its own
+    block-table row; that row must cover the shard's local length
+    [PR565, review follow-up: the page table must cover the largest local KV
+    shard; PR50484, Summary: each DCP rank keeps its own slice of the
+    context]."""
+    j = np.arange(int(n), dtype=np.int64)
+    blocks = np.asarray(shard_table_row, dtype=np.int64)[j // block_size]
+    return blocks * block_size + j % block_size
+
+
 def gather_latents(kv_cache_bits: np.ndarray, table_row: np.ndarray, block_size: int,
                    positions: np.ndarray) -> np.ndarray:
     """float64 [len(positions), 576] latent rows of the given logical positions."""
@@ -173,8 +186,11 @@ def shard_partial(s: np.ndarray, values: np.ndarray):
 
 
 def decode_partial_row(q_heads: np.ndarray, kv_cache_bits: np.ndarray, table_row: np.ndarray,
-                       block_size: int, L: int, D: int, I: int, scale: float, padding: bool):
+                       block_size: int, L: int, D: int, I: int, scale: float, padding: bool,
+                       local: bool = False):
     """(O [D, H, 512], lse [D, H]) of one query row over its own L tokens.
+    table_row is the request's block-table row, or with ``local`` its D
+    per-shard rows [D, W] (the shard's tokens gathered by local index).
 
     Empty shards and padding rows are masked at the source: lse = -inf,
     O = NaN [PR50484, Summary: empty-KV-shard masking; PRHUB, implementation
@@ -189,7 +205,12 @@ def decode_partial_row(q_heads: np.ndarray, kv_cache_bits: np.ndarray, table_row
         pos = shard_positions(L, d, D, I)
         if pos.size == 0:
             continue
-        kv = gather_latents(kv_cache_bits, table_row, block_size, pos)
+        if local:
+            nb, bs, kd = kv_cache_bits.shape
+            rows = physical_rows_local(table_row[d], block_size, pos.size)
+            kv = bf16_to_f64(kv_cache_bits.reshape(nb * bs, kd)[rows])
+        else:
+            kv = gather_latents(kv_cache_bits, table_row, block_size, pos)
         O[d], lse[d] = shard_partial(scores(q, kv, scale), kv[:, :LATENT])
     return O, lse
 
@@ -198,19 +219,25 @@ def decode_partial(inp: dict, rows=None):
     """Oracle of ``dcp_mla_decode_partial`` on a workload dict from
     ``workloads.make_decode_inputs``, for the listed rows (default all).
 
-    Returns (O_part [D, R, H, 512], lse_part [D, R, H], rows).
+    Returns (O_part [D, R, H, 512], lse_part [D, R, H], rows).  With
+    ``inp["layout"] == "local"`` the block table is [D, B, W]: each shard's
+    own table (the per-shard layout).
     """
     T, H, D = inp["T"], inp["H"], inp["D"]
+    local = inp.get("layout", "global") == "local"
     req, L, padding = row_lengths(inp["seq_lens"], inp["query_start_loc"], T)
     rows = np.arange(T) if rows is None else np.asarray(rows, dtype=np.int64)
     O = np.full((D, len(rows), H, LATENT), np.nan)
     lse = np.full((D, len(rows), H), -np.inf)
     for j, r in enumerate(rows):
         b = req[r]
-        table_row = inp["block_table"][b] if b >= 0 else None
+        if b < 0:
+            table_row = None
+        else:
+            table_row = inp["block_table"][:, b] if local else inp["block_table"][b]
         O[:, j], lse[:, j] = decode_partial_row(
             inp["q"][r], inp["kv_cache"], table_row, inp["block_size"], int(L[r]),
-            D, inp["interleave"], inp["scale"], bool(padding[r]))
+            D, inp["interleave"], inp["scale"], bool(padding[r]), local=local)
     return O, lse, rows
 
 

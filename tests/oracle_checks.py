@@ -340,3 +340,49 @@ def check_concat_cache_feeds_the_walker(o):
     got = o.gather_latents(cache, table, bs, np.array([L]))
     want = o.bf16_to_f64(np.concatenate([kv_c, k_pe], axis=-1))
     assert np.array_equal(got, want)
+
+
+# ---------------------------------------------------------------------------
+# per-shard (rank-local) block tables and shared prefixes
+# ---------------------------------------------------------------------------
+LAYOUT_CASES = [
+    dict(B=2, seq_lens=(300, 77), H=4, block_size=16, D=4, interleave=3),
+    dict(B=3, seq_lens=(130, 1, 64), q_len=2, H=2, block_size=8, D=2, interleave=4, extra_rows=1),
+    dict(B=2, seq_lens=(200, 150), H=2, block_size=16, D=8, interleave=1, prefix_len=100, shared_prefix=True),
+]
+
+
+def check_local_layout_matches_global(o):
+    """The same logical context stored in the per-shard layout or in the
+    global layout gives the same partials: the local walker reads exactly the
+    positions each shard owns, in the same order as the global one."""
+    import workloads as wl
+    for i, kw in enumerate(LAYOUT_CASES):
+        g = wl.make_decode_inputs(wl.DecodeSpec("g%d" % i, seed=80 + i, layout="global", **kw))
+        l = wl.make_decode_inputs(wl.DecodeSpec("l%d" % i, seed=80 + i, layout="local", **kw))
+        assert l["block_table"].shape[:2] == (kw["D"], kw["B"])
+        Og, lg, _ = o.decode_partial(g)
+        Ol, ll, _ = o.decode_partial(l)
+        assert np.array_equal(lg, ll), i
+        assert np.array_equal(np.isnan(Og), np.isnan(Ol)), i
+        live = ~np.isnan(Og)
+        assert np.array_equal(Og[live], Ol[live]), i
+
+
+def check_shared_prefix(o):
+    """Two requests sharing a prefix: the prefix tokens are the same values in
+    both, the blocks that hold only prefix tokens are the same blocks, and
+    shard partials over a context of exactly the prefix agree between them."""
+    import workloads as wl
+    spec = wl.DecodeSpec("sp", seed=90, B=2, seq_lens=(200, 150), H=3, block_size=16, D=4, interleave=1,
+                         prefix_len=96, shared_prefix=True, q_len=1)
+    inp = wl.make_decode_inputs(spec)
+    t = inp["block_table"]
+    assert np.array_equal(t[0, :6], t[1, :6]) and not np.intersect1d(t[0, 6:13], t[1, 6:10]).size
+    pos = np.arange(96)
+    a = o.gather_latents(inp["kv_cache"], t[0], 16, pos)
+    b = o.gather_latents(inp["kv_cache"], t[1], 16, pos)
+    assert np.array_equal(a, b)
+    # the suffixes differ
+    assert not np.array_equal(o.gather_latents(inp["kv_cache"], t[0], 16, np.arange(96, 150)),
+                              o.gather_latents(inp["kv_cache"], t[1], 16, np.arange(96, 150)))

@@ -100,3 +100,11 @@ def test_concat_cache_is_cat_and_scatter():
 
 def test_concat_cache_feeds_the_walker():
     C.check_concat_cache_feeds_the_walker(oracle)
+
+
+def test_local_layout_matches_global():
+    C.check_local_layout_matches_global(oracle)
+
+
+def test_shared_prefix_blocks_and_values():
+    C.check_shared_prefix(oracle)

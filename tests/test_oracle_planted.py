@@ -123,3 +123,13 @@ def test_concat_cache_negative_slot_written_is_caught(monkeypatch):
 def test_concat_cache_dropped_q_pe_is_caught(monkeypatch):
     monkeypatch.setattr(O, "concat_cache", _concat_variant(drop_pe=True))
     _fails(C.check_concat_cache)
+
+
+def test_local_walker_by_position_is_caught(monkeypatch):
+    # a local walker that indexes the shard's table by global position
+    def bad(shard_table_row, block_size, n):
+        j = np.arange(int(n), dtype=np.int64) * 2
+        blocks = np.asarray(shard_table_row, dtype=np.int64)[np.minimum(j // block_size, len(shard_table_row) - 1)]
+        return blocks * block_size + j % block_size
+    monkeypatch.setattr(O, "physical_rows_local", bad)
+    _fails(C.check_local_layout_matches_global)

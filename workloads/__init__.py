@@ -75,6 +75,13 @@ class DecodeSpec:
     spare_cols: int = 2          # poisoned (-1) block-table columns past the widest request
     extra_rows: int = 0          # rows past query_start_loc[B] (no request: padding)
     tail_fill_nan: bool = True   # cache slots past seq_len hold NaN
+    # "global": one block table per request over all positions; "local": the
+    # per-shard layout, each shard's tokens stored densely in its own blocks
+    # (block_table [D, B, W])
+    layout: str = "global"
+    # the first prefix_len tokens of every request are the same tokens (drawn
+    # once) stored in the same blocks (those holding only prefix tokens)
+    shared_prefix: bool = False
 
     def q_lens(self) -> Tuple[int, ...]:
         if isinstance(self.q_len, int):
@@ -115,19 +122,20 @@ def _threads() -> int:
 
 def _fill_request(kv_flat: np.ndarray, phys_rows: np.ndarray, spec: DecodeSpec,
                   b: int, L: int) -> None:
-    """Draw request b's L latent rows in logical order and store them."""
+    """Draw request b's L latent rows in logical order and store them.  With a
+    shared prefix every request draws its prefix from request 0's stream."""
     jobs = []
     if spec.prefix_len is not None and spec.prefix_len < L:
-        segs = [(0, spec.prefix_len, _S_KV), (spec.prefix_len, L, _S_KV_SUFFIX)]
+        segs = [(0, spec.prefix_len, _S_KV, 0 if spec.shared_prefix else b), (spec.prefix_len, L, _S_KV_SUFFIX, b)]
     else:
-        segs = [(0, L, _S_KV)]
-    for lo, hi, stream in segs:
+        segs = [(0, L, _S_KV, b)]
+    for lo, hi, stream, owner in segs:
         for c, start in enumerate(range(lo, hi, CHUNK)):
-            jobs.append((stream, c, start, min(hi, start + CHUNK)))
+            jobs.append((stream, owner, c, start, min(hi, start + CHUNK)))
 
     def work(job):
-        stream, c, start, stop = job
-        rng = np.random.default_rng([spec.seed, stream, b, c])
+        stream, owner, c, start, stop = job
+        rng = np.random.default_rng([spec.seed, stream, owner, c])
         x = rng.standard_normal((stop - start, KDIM), dtype=np.float32)
         kv_flat[phys_rows[start:stop]] = f32_to_bf16_bits(x)
 
@@ -158,18 +166,8 @@ def make_decode_inputs(spec: DecodeSpec, kv_rows=None) -> dict:
     qsl = np.zeros(B + 1, dtype=np.int32)
     qsl[1:] = np.cumsum(qlens)
     T = int(qsl[-1]) + spec.extra_rows
-    nblk = (seq.astype(np.int64) + bs - 1) // bs
-    num_blocks = max(1, int(nblk.sum()))
-    W = int(nblk.max(initial=0)) + spec.spare_cols
-    W = max(W, 1)
-
-    perm = np.random.default_rng([spec.seed, _S_TABLE]).permutation(num_blocks).astype(np.int32)
-    table = np.full((B, W), -1, dtype=np.int32)
-    off = 0
-    for b in range(B):
-        n = int(nblk[b])
-        table[b, :n] = perm[off:off + n]
-        off += n
+    placement = _place_global if spec.layout == "global" else _place_local
+    table, phys_of, num_blocks = placement(spec, seq)
 
     kv = np.empty((num_blocks, bs, KDIM), dtype=np.uint16)
     if spec.tail_fill_nan:
@@ -182,7 +180,7 @@ def make_decode_inputs(spec: DecodeSpec, kv_rows=None) -> dict:
         if L == 0:
             continue
         pos = np.arange(L, dtype=np.int64)
-        phys = table[b, pos // bs].astype(np.int64) * bs + pos % bs
+        phys = phys_of(b, pos)
         if kv_rows is None:
             _fill_request(kv_flat, phys, spec, b, L)
         else:
@@ -195,8 +193,93 @@ def make_decode_inputs(spec: DecodeSpec, kv_rows=None) -> dict:
         query_start_loc=qsl, B=B, T=T, H=spec.H, D=spec.D,
         interleave=spec.interleave, block_size=bs, scale=float(spec.scale),
         max_seq_len=int(seq.max(initial=0)), max_q_len=int(qlens.max(initial=0)),
-        num_blocks=num_blocks,
+        num_blocks=num_blocks, layout=spec.layout,
     )
+
+
+def _shared_blocks(spec: DecodeSpec, counts: np.ndarray) -> np.ndarray:
+    """Per request, how many leading blocks hold only shared-prefix tokens
+    (counts[b] = prefix tokens of request b in the table row's order)."""
+    if not spec.shared_prefix or spec.prefix_len is None:
+        return np.zeros_like(counts)
+    return counts // spec.block_size
+
+
+def _allocate(spec: DecodeSpec, nblk: np.ndarray, nshared: np.ndarray, W: int, rng_stream: int):
+    """Block ids for a set of table rows (nblk[i] blocks each; the first
+    nshared[i] of them are the rows' common prefix blocks, allocated once),
+    drawn from a random permutation of all blocks.  Returns (table rows
+    [len(nblk), W] with -1 in unused columns, number of blocks)."""
+    shared = int(nshared.max(initial=0))
+    own = nblk - np.minimum(nshared, nblk)
+    num_blocks = max(1, shared + int(own.sum()))
+    key = [spec.seed, _S_TABLE] if rng_stream == 0 else [spec.seed, _S_TABLE, rng_stream]
+    perm = np.random.default_rng(key).permutation(num_blocks).astype(np.int32)
+    rows = np.full((len(nblk), max(W, 1)), -1, dtype=np.int32)
+    off = shared
+    for i in range(len(nblk)):
+        ns = int(min(nshared[i], nblk[i]))
+        rows[i, :ns] = perm[:ns]
+        n = int(nblk[i]) - ns
+        rows[i, ns:ns + n] = perm[off:off + n]
+        off += n
+    return rows, num_blocks
+
+
+def _place_global(spec: DecodeSpec, seq: np.ndarray):
+    """One table row per request: position p of request b lives in row
+    table[b, p // bs] * bs + p % bs."""
+    bs = spec.block_size
+    nblk = (seq.astype(np.int64) + bs - 1) // bs
+    pre = np.minimum(seq.astype(np.int64), spec.prefix_len or 0)
+    W = int(nblk.max(initial=0)) + spec.spare_cols
+    table, num_blocks = _allocate(spec, nblk, _shared_blocks(spec, pre), W, 0)
+
+    def phys_of(b, pos):
+        return table[b, pos // bs].astype(np.int64) * bs + pos % bs
+    return table, phys_of, num_blocks
+
+
+def _place_local(spec: DecodeSpec, seq: np.ndarray):
+    """The per-shard (DCP rank-local) layout: shard d stores the positions it
+    owns, dealt round-robin to the D shards in runs of I, densely in order;
+    its j-th token of request b lives in row table[d, b, j // bs] * bs +
+    j % bs.  This is how each rank's own cache holds its share of the
+    context; the placement is input construction, checked against the global
+    layout by the oracle's tests."""
+    bs, D, I = spec.block_size, spec.D, spec.interleave
+    B = len(seq)
+    owners, local_idx, counts = [], [], np.zeros((D, B), dtype=np.int64)
+    for b in range(B):
+        p = np.arange(int(seq[b]), dtype=np.int64)
+        run = p // I
+        d = run % D
+        j = (run // D) * I + p % I  # rank of p among its shard's positions
+        owners.append(d)
+        local_idx.append(j)
+        for dd in range(D):
+            counts[dd, b] = int((d == dd).sum())
+    nblk = (counts + bs - 1) // bs
+    pre_counts = np.zeros((D, B), dtype=np.int64)
+    if spec.shared_prefix and spec.prefix_len:
+        for b in range(B):
+            k = min(int(seq[b]), spec.prefix_len)
+            for dd in range(D):
+                pre_counts[dd, b] = int((owners[b][:k] == dd).sum())
+    W = int(nblk.max(initial=0)) + spec.spare_cols
+    num_blocks = 0
+    tables = np.full((D, B, max(W, 1)), -1, dtype=np.int32)
+    # each shard's blocks are a contiguous range of one cache (on one GPU the
+    # D rank-local caches are partitions of one array), permuted within it
+    for dd in range(D):
+        r, n = _allocate(spec, nblk[dd], _shared_blocks(spec, pre_counts[dd]), W, 1 + dd)
+        tables[dd] = np.where(r >= 0, r + num_blocks, -1)
+        num_blocks += n
+
+    def phys_of(b, pos):
+        d, j = owners[b][pos], local_idx[b][pos]
+        return tables[d, b, j // bs].astype(np.int64) * bs + j % bs
+    return tables, phys_of, num_blocks
 
 
 def combine_masks(D: int, T: int, seed: int, empty_frac: float = 0.10,
