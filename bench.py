@@ -218,10 +218,15 @@ def barrier():
 
 def workload_config(spec, inp, n_gpus: int) -> dict:
     """The `config` object of a bench line, the same for both arms."""
-    return {"workload": spec.name, "B": spec.B, "seq_len": int(inp["max_seq_len"]), "H": spec.H,
-            "D": spec.D, "interleave": spec.interleave, "block_size": spec.block_size,
-            "q_len": int(inp["max_q_len"]), "parallelism": "replicas" if n_gpus > 1 else "single",
-            "l2": "flushed before every timed step (512 MB write, untimed)"}
+    cfg = {"workload": spec.name, "B": spec.B, "seq_len": int(inp["max_seq_len"]), "H": spec.H,
+           "D": spec.D, "interleave": spec.interleave, "block_size": spec.block_size,
+           "q_len": int(inp["max_q_len"]), "parallelism": "replicas" if n_gpus > 1 else "single",
+           "l2": "flushed before every timed step (512 MB write, untimed)"}
+    if spec.layout != "global":
+        cfg["block_tables"] = "per-shard (rank-local)"
+    if spec.shared_prefix:
+        cfg["shared_prefix"] = spec.prefix_len
+    return cfg
 
 
 def run_reference(args, spec):
@@ -527,7 +532,8 @@ def run_gb300(args, spec):
     # ---- the other workloads: decode records and the combine sweep ----
     if rank == 0 and not args.headline_only:
         recs = {}
-        for other in (wl.BATCHED_B64, wl.SPEC_VERIFY_B32):
+        for other in (wl.BATCHED_B64, wl.SPEC_VERIFY_B32, wl.LONG_120K_B2_PREFIX, wl.LONG_120K_B2_PREFIX_LOCAL,
+                      wl.BATCHED_B64_LOCAL):
             ob = DecodeBench(other, dev, use_graphs=not args.eager)
             osteps = max(5, min(args.steps, 20))
             d_ms, c_ms = ob.timed(osteps, 3, flush)

@@ -218,6 +218,41 @@ dcp_status_t dcp_lse_combine(
     void* out, dcp_dtype_t out_dtype, float* out_lse, void* stream);
 
 /*
+ * dcp_mla_decode_partial over per-shard (DCP rank-local) block tables: each
+ * shard stores only the tokens it owns, densely and in order, in its own
+ * blocks, as each rank's own cache does ["[Kimi-K3] DCP support", Summary:
+ * each DCP rank keeps its slice of the context; PR565, review follow-up: the
+ * plan's page table must cover the largest local KV shard].  Same
+ * arguments, results and errors as dcp_mla_decode_partial, except:
+ *
+ *   block_table     int32 [D, B, bt_width]: shard d's j-th local token of
+ *                   request b lives in cache row
+ *                   table[d, b, j / block_size] * block_size + j % block_size.
+ *                   Request rows are bt_stride elements apart (>= bt_width),
+ *                   shard tables bt_shard_stride apart
+ *                   (>= (B - 1) * bt_stride + bt_width, else
+ *                   DCP_ERR_INVALID_ARG).  Only the columns a shard's local
+ *                   tokens reach are read.
+ *   bt_width        must cover the largest local shard (shard 0):
+ *                   ceil(local_len(max_seq_len, 0, D, interleave) /
+ *                   block_size) <= bt_width, else DCP_ERR_TABLE_TOO_NARROW.
+ *
+ * The shard of a token and its local index follow the same interleave rule
+ * (dcp_shard_of, dcp_local_len).  The workspace is sized by
+ * dcp_decode_workspace_size as for the global layout.
+ */
+dcp_status_t dcp_mla_decode_partial_local(
+    const void* q, int64_t q_stride_tok,
+    const void* kv_cache, int32_t num_blocks, int32_t block_size,
+    const int32_t* block_table, int32_t bt_width, int64_t bt_stride, int64_t bt_shard_stride,
+    const int32_t* seq_lens, const int32_t* query_start_loc,
+    int32_t B, int32_t T, int32_t H, int32_t max_seq_len, int32_t max_q_len,
+    int32_t D, int32_t interleave, float scale,
+    float* O_part, float* lse_part,
+    void* workspace, size_t workspace_bytes,
+    int32_t* dev_error, void* stream);
+
+/*
  * The decode step before attention, fused into one launch ["[Kimi-K3] DCP
  * support" summary on prhub.com.cn, key snippet "Decode: latent multi-query
  * attention": _decode_concat_cache builds the decode query and writes this

@@ -55,6 +55,9 @@ EXPORTS = [
      [_P, _I64, _P, _I32, _I32, _P, _I32, _I64, _P, _P, _I32, _I32, _I32, _I32, _I32, _I32, _I32, _F,
       _P, _P, _P, _SZ, _P, _P]),
     ("dcp_lse_combine", ctypes.c_int, [_P, _P, _P, _P, _I32, _I32, _I32, _I32, _P, ctypes.c_int, _P, _P]),
+    ("dcp_mla_decode_partial_local", ctypes.c_int,
+     [_P, _I64, _P, _I32, _I32, _P, _I32, _I64, _I64, _P, _P, _I32, _I32, _I32, _I32, _I32, _I32, _I32, _F,
+      _P, _P, _P, _SZ, _P, _P]),
     ("dcp_decode_concat_cache", ctypes.c_int,
      [_P, _I64, _I64, _P, _I64, _I64, _P, _I64, _P, _I64, _P, _I32, _I32, _P, _I64, _P, _I64, _P, _P]),
     ("dcp_mla_decode_partial_noalloc", ctypes.c_int,
@@ -162,7 +165,8 @@ def _need(t: torch.Tensor, name: str, dtype, contiguous=True):
         raise ValueError("%s must be contiguous" % name)
 
 
-def _decode_geometry(q, kv_cache, block_table, seq_lens, query_start_loc, O_part, lse_part, D: int):
+def _decode_geometry(q, kv_cache, block_table, seq_lens, query_start_loc, O_part, lse_part, D: int,
+                     local: bool = False):
     """Validate the decode arguments both decode entry points share and
     return (B, T, H).  Every size the kernels index by is checked here,
     because the C ABI receives bare pointers: a short block table or a
@@ -181,14 +185,17 @@ def _decode_geometry(q, kv_cache, block_table, seq_lens, query_start_loc, O_part
         raise ValueError("q must be [T, H, 576] with contiguous heads")
     if kv_cache.dim() != 3 or kv_cache.shape[2] != KV_DIM:
         raise ValueError("kv_cache must be [num_blocks, block_size, 576]")
-    if block_table.dim() != 2 or block_table.stride(1) != 1:
+    if local:
+        if block_table.dim() != 3 or block_table.stride(2) != 1 or block_table.shape[0] != D:
+            raise ValueError("block_table must be [D, B, W] with unit column stride")
+    elif block_table.dim() != 2 or block_table.stride(1) != 1:
         raise ValueError("block_table must be [B, W] with unit column stride")
     if seq_lens.dim() != 1 or query_start_loc.dim() != 1:
         raise ValueError("seq_lens and query_start_loc must be 1-D")
     T, H = q.shape[0], q.shape[1]
     B = seq_lens.shape[0]
-    if query_start_loc.shape[0] != B + 1 or block_table.shape[0] != B:
-        raise ValueError("seq_lens [B], query_start_loc [B + 1] and block_table [B, W] disagree on B")
+    if query_start_loc.shape[0] != B + 1 or block_table.shape[-2] != B:
+        raise ValueError("seq_lens [B], query_start_loc [B + 1] and block_table [.., B, W] disagree on B")
     if tuple(O_part.shape) != (D, T, H, LATENT_DIM) or tuple(lse_part.shape) != (D, T, H):
         raise ValueError("O_part must be [D, T, H, 512] and lse_part [D, T, H]")
     for name, t, dtype, contiguous in args:
@@ -251,6 +258,29 @@ def dcp_mla_decode_partial(q, kv_cache, block_table, seq_lens, query_start_loc, 
             max_seq_len, max_q_len, D, interleave, scale, _ptr(O_part), _ptr(lse_part), _ptr(workspace),
             ws_bytes, _ptr(dev_error), _stream(stream))
     _check(st, "dcp_mla_decode_partial")
+
+
+def dcp_mla_decode_partial_local(q, kv_cache, block_table, seq_lens, query_start_loc, O_part, lse_part, *,
+                                 D: int, interleave: int, scale: float, max_seq_len: int, max_q_len: int,
+                                 workspace: Optional[torch.Tensor] = None,
+                                 dev_error: Optional[torch.Tensor] = None, stream=None) -> None:
+    """dcp_mla_decode_partial over per-shard tables: block_table int32
+    [D, B, W], shard d's j-th local token of request b in row
+    block_table[d, b, j // bs] * bs + j % bs."""
+    B, T, H = _decode_geometry(q, kv_cache, block_table, seq_lens, query_start_loc, O_part, lse_part, D,
+                               local=True)
+    _need_opt(workspace, "workspace", allow_empty=True)
+    if workspace is not None and workspace.numel() == 0:
+        workspace = None
+    _need_opt(dev_error, "dev_error", torch.int32)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    with _Range("dcp_mla_decode_partial_local"):
+        st = lib().dcp_mla_decode_partial_local(
+            _ptr(q), q.stride(0), _ptr(kv_cache), kv_cache.shape[0], kv_cache.shape[1], _ptr(block_table),
+            block_table.shape[2], block_table.stride(1), block_table.stride(0), _ptr(seq_lens),
+            _ptr(query_start_loc), B, T, H, max_seq_len, max_q_len, D, interleave, scale, _ptr(O_part),
+            _ptr(lse_part), _ptr(workspace), ws_bytes, _ptr(dev_error), _stream(stream))
+    _check(st, "dcp_mla_decode_partial_local")
 
 
 def dcp_mla_decode_partial_noalloc(q, kv_cache, block_table, seq_lens, query_start_loc, O_part, lse_part, *,
@@ -372,21 +402,24 @@ def decode_partial(q, kv_cache, block_table, seq_lens, query_start_loc, D: int, 
                    scale: float, max_seq_len: Optional[int] = None, max_q_len: Optional[int] = None,
                    dev_error: Optional[torch.Tensor] = None, stream=None):
     """Allocating form: returns (O_part fp32 [D, T, H, 512], lse_part fp32 [D, T, H]).
+    A 3-D block_table [D, B, W] selects the per-shard layout
+    (dcp_mla_decode_partial_local).
 
     ``max_seq_len``/``max_q_len`` default to the bounds implied by the table
     width and the row count (no device->host copy)."""
     T, H = q.shape[0], q.shape[1]
     B = seq_lens.shape[0]
+    local = block_table.dim() == 3
     if max_seq_len is None:
-        max_seq_len = block_table.shape[1] * kv_cache.shape[1]
+        max_seq_len = block_table.shape[-1] * kv_cache.shape[1] * (D if local else 1)
     if max_q_len is None:
         max_q_len = max(1, T)
     O = torch.empty((D, T, H, LATENT_DIM), dtype=torch.float32, device=q.device)
     lse = torch.empty((D, T, H), dtype=torch.float32, device=q.device)
     ws = decode_workspace(B, T, H, D, max_seq_len, max_q_len, q.device)
-    dcp_mla_decode_partial(q, kv_cache, block_table, seq_lens, query_start_loc, O, lse, D=D,
-                           interleave=interleave, scale=scale, max_seq_len=max_seq_len,
-                           max_q_len=max_q_len, workspace=ws, dev_error=dev_error, stream=stream)
+    entry = dcp_mla_decode_partial_local if local else dcp_mla_decode_partial
+    entry(q, kv_cache, block_table, seq_lens, query_start_loc, O, lse, D=D, interleave=interleave, scale=scale,
+          max_seq_len=max_seq_len, max_q_len=max_q_len, workspace=ws, dev_error=dev_error, stream=stream)
     return O, lse
 
 

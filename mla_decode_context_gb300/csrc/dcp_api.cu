@@ -149,13 +149,15 @@ size_t dcp_decode_workspace_size(int32_t B, int32_t T, int32_t H, int32_t D, int
   return dcp::split_workspace_bytes(p, T, H, D) + dcp::order_workspace_bytes(p, T, D);
 }
 
-dcp_status_t dcp_mla_decode_partial(const void* q, int64_t q_stride_tok, const void* kv_cache,
-                                    int32_t num_blocks, int32_t block_size, const int32_t* block_table,
-                                    int32_t bt_width, int64_t bt_stride, const int32_t* seq_lens,
-                                    const int32_t* query_start_loc, int32_t B, int32_t T, int32_t H,
-                                    int32_t max_seq_len, int32_t max_q_len, int32_t D, int32_t interleave,
-                                    float scale, float* O_part, float* lse_part, void* workspace,
-                                    size_t workspace_bytes, int32_t* dev_error, void* stream) {
+}  // extern "C"
+
+static dcp_status_t decode_partial_impl(const void* q, int64_t q_stride_tok, const void* kv_cache,
+                                        int32_t num_blocks, int32_t block_size, const int32_t* block_table,
+                                        int32_t bt_width, int64_t bt_stride, bool local, int64_t bt_shard_stride,
+                                        const int32_t* seq_lens, const int32_t* query_start_loc, int32_t B,
+                                        int32_t T, int32_t H, int32_t max_seq_len, int32_t max_q_len, int32_t D,
+                                        int32_t interleave, float scale, float* O_part, float* lse_part,
+                                        void* workspace, size_t workspace_bytes, int32_t* dev_error, void* stream) {
   if (B < 0 || T < 0 || H < 1 || H > 1024 || D < 1 || D > DCP_MAX_SHARDS || interleave < 1 ||
       max_seq_len < 0 || max_q_len < 1 || !std::isfinite(scale))
     return DCP_ERR_INVALID_ARG;
@@ -167,8 +169,12 @@ dcp_status_t dcp_mla_decode_partial(const void* q, int64_t q_stride_tok, const v
     return DCP_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(kv_cache) || !aligned16(O_part) || (q_stride_tok % 8) != 0)
     return DCP_ERR_MISALIGNED;
-  if ((static_cast<int64_t>(max_seq_len) + block_size - 1) / block_size > bt_width)
-    return DCP_ERR_TABLE_TOO_NARROW;
+  if (local && bt_shard_stride < static_cast<int64_t>(B - 1) * bt_stride + bt_width)
+    return DCP_ERR_INVALID_ARG;  // shards' tables would overlap
+  // a table row covers the longest sequence (global layout) or the largest
+  // local shard, shard 0 (per-shard layout)
+  const int64_t covered = local ? dcp::local_len(max_seq_len, 0, D, interleave) : max_seq_len;
+  if ((covered + block_size - 1) / block_size > bt_width) return DCP_ERR_TABLE_TOO_NARROW;
 
   const DecodeLaunch launch =
       decode_launch(T, H, D, interleave, max_seq_len, workspace != nullptr, workspace_bytes);
@@ -187,6 +193,8 @@ dcp_status_t dcp_mla_decode_partial(const void* q, int64_t q_stride_tok, const v
   a.block_table = block_table;
   a.bt_width = bt_width;
   a.bt_stride = bt_stride;
+  a.local_tables = local ? 1 : 0;
+  a.bt_shard_stride = local ? bt_shard_stride : 0;
   a.seq_lens = seq_lens;
   a.qsl = query_start_loc;
   a.B = B; a.T = T; a.H = H;
@@ -232,6 +240,34 @@ dcp_status_t dcp_mla_decode_partial(const void* q, int64_t q_stride_tok, const v
     if (e != cudaSuccess) return DCP_ERR_CUDA;
   }
   return DCP_OK;
+}
+
+
+extern "C" {
+
+dcp_status_t dcp_mla_decode_partial(const void* q, int64_t q_stride_tok, const void* kv_cache,
+                                    int32_t num_blocks, int32_t block_size, const int32_t* block_table,
+                                    int32_t bt_width, int64_t bt_stride, const int32_t* seq_lens,
+                                    const int32_t* query_start_loc, int32_t B, int32_t T, int32_t H,
+                                    int32_t max_seq_len, int32_t max_q_len, int32_t D, int32_t interleave,
+                                    float scale, float* O_part, float* lse_part, void* workspace,
+                                    size_t workspace_bytes, int32_t* dev_error, void* stream) {
+  return decode_partial_impl(q, q_stride_tok, kv_cache, num_blocks, block_size, block_table, bt_width, bt_stride,
+                             false, 0, seq_lens, query_start_loc, B, T, H, max_seq_len, max_q_len, D, interleave,
+                             scale, O_part, lse_part, workspace, workspace_bytes, dev_error, stream);
+}
+
+dcp_status_t dcp_mla_decode_partial_local(const void* q, int64_t q_stride_tok, const void* kv_cache,
+                                          int32_t num_blocks, int32_t block_size, const int32_t* block_table,
+                                          int32_t bt_width, int64_t bt_stride, int64_t bt_shard_stride,
+                                          const int32_t* seq_lens, const int32_t* query_start_loc, int32_t B,
+                                          int32_t T, int32_t H, int32_t max_seq_len, int32_t max_q_len, int32_t D,
+                                          int32_t interleave, float scale, float* O_part, float* lse_part,
+                                          void* workspace, size_t workspace_bytes, int32_t* dev_error,
+                                          void* stream) {
+  return decode_partial_impl(q, q_stride_tok, kv_cache, num_blocks, block_size, block_table, bt_width, bt_stride,
+                             true, bt_shard_stride, seq_lens, query_start_loc, B, T, H, max_seq_len, max_q_len, D,
+                             interleave, scale, O_part, lse_part, workspace, workspace_bytes, dev_error, stream);
 }
 
 int32_t dcp_decode_kernel_launches(int32_t B, int32_t T, int32_t H, int32_t D, int32_t interleave,

@@ -72,7 +72,8 @@ decode_simt_kernel(DecodeArgs a) {
       sm.q[i / kKDim][i % kKDim] = v;
     }
     const float sl2 = a.scale * kLog2e;
-    const int32_t* trow = a.block_table + static_cast<int64_t>(ri.b) * a.bt_stride;
+    const int32_t* trow = a.block_table + static_cast<int64_t>(ri.b) * a.bt_stride +
+                          (a.local_tables ? static_cast<int64_t>(d) * a.bt_shard_stride : 0);
 
     for (int32_t t0 = lo; t0 < hi; t0 += kTile) {
       __syncthreads();  // previous tile fully consumed (and q staged)
@@ -80,7 +81,8 @@ decode_simt_kernel(DecodeArgs a) {
         const int32_t j = t0 + threadIdx.x;
         int64_t phys = -1;
         if (j < hi) {
-          const int64_t p = local_to_global(j, d, a.D, a.I);
+          // table index: the shard token's position, or its local index (per-shard layout)
+          const int64_t p = a.local_tables ? j : local_to_global(j, d, a.D, a.I);
           const int32_t blk = __ldg(trow + p / a.block_size);
           if (blk >= 0 && blk < a.num_blocks)
             phys = static_cast<int64_t>(blk) * a.block_size + p % a.block_size;

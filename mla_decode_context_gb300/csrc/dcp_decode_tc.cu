@@ -375,7 +375,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(DecodeArgs a) {
     TR_LAP(4, 6);  // score warps 0-7: Q load
   }
 
-  const int32_t* trow = a.block_table + static_cast<int64_t>(ri.b) * a.bt_stride;
+  // the request's table row (global layout) or this shard's row of it (per-shard layout)
+  const int32_t* trow = a.block_table + static_cast<int64_t>(ri.b) * a.bt_stride +
+                        (a.local_tables ? static_cast<int64_t>(d) * a.bt_shard_stride : 0);
   const uint32_t smem_base = smem_u32(smem);
   int pdone = 0;  // value, warps 0-3: P tiles received
 
@@ -411,7 +413,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(DecodeArgs a) {
       for (int e = 0; e < 2; ++e) {
         const int32_t l = lo + jj * kTile + (e ? row1 : row0);
         in_n[e] = l < hi;
-        pos_n[e] = in_n[e] ? (l / a.I) * DI + dI + l % a.I : 0;
+        // the table index: the shard token's position, or (per-shard
+        // layout) the local token index itself
+        pos_n[e] = in_n[e] ? (a.local_tables ? l : (l / a.I) * DI + dI + l % a.I) : 0;
         blk_n[e] = in_n[e] ? __ldg(trow + pos_n[e] / a.block_size) : -1;
       }
     };

@@ -17,7 +17,13 @@ struct DecodeArgs {
   int32_t num_blocks, block_size;
   const int32_t* block_table;
   int32_t bt_width;
-  int64_t bt_stride;
+  int64_t bt_stride;        // elements between requests' table rows
+  // per-shard (rank-local) tables: block_table is [D, B, W] with shard d's
+  // rows bt_shard_stride elements after shard d - 1's, and shard d's j-th
+  // local token lives in row table[d, b, j / block_size] * block_size +
+  // j % block_size; otherwise one table row per request over positions
+  int32_t local_tables;
+  int64_t bt_shard_stride;
   const int32_t* seq_lens;
   const int32_t* qsl;
   int32_t B, T, H, max_seq_len, max_q_len, D, I;

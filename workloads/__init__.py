@@ -110,10 +110,21 @@ BATCHED_B64 = DecodeSpec("batched_b64_d8_i64", seed=2, B=64,
 SPEC_VERIFY_B32 = DecodeSpec("spec_verify_b32_q4_d8_i1", seed=3, B=32,
                              seq_lens=("uniform", 8192, 65536), q_len=4, H=128,
                              block_size=64, D=8, interleave=1)
+# the 120k workload as two requests sharing the 114,000-token prefix (the
+# blocks that hold only prefix tokens are shared), in the global layout and in
+# the per-shard (rank-local) layout
+LONG_120K_B2_PREFIX = DecodeSpec("long_ctx_120k_b2_shared_prefix_d8_i1", seed=6, B=2, seq_lens=(120_000, 120_000),
+                                 H=128, block_size=64, D=8, interleave=1, prefix_len=114_000, shared_prefix=True)
+LONG_120K_B2_PREFIX_LOCAL = DecodeSpec("long_ctx_120k_b2_shared_prefix_d8_i1_local", seed=6, B=2,
+                                       seq_lens=(120_000, 120_000), H=128, block_size=64, D=8, interleave=1,
+                                       prefix_len=114_000, shared_prefix=True, layout="local")
+BATCHED_B64_LOCAL = DecodeSpec("batched_b64_d8_i64_local", seed=2, B=64, seq_lens=("uniform", 1024, 32768), H=128,
+                               block_size=64, D=8, interleave=64, layout="local")
 COMBINE_SWEEP = [(D, T) for D in (2, 4, 8) for T in (1, 64, 1024, 4096)]
 COMBINE_H = 128
 
-DECODE_WORKLOADS = {s.name: s for s in (TINY, LONG_120K, BATCHED_B64, SPEC_VERIFY_B32)}
+DECODE_WORKLOADS = {s.name: s for s in (TINY, LONG_120K, BATCHED_B64, SPEC_VERIFY_B32, LONG_120K_B2_PREFIX,
+                                         LONG_120K_B2_PREFIX_LOCAL, BATCHED_B64_LOCAL)}
 
 
 def _threads() -> int:
