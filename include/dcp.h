@@ -225,21 +225,31 @@ dcp_status_t dcp_lse_combine(
  * plan's page table must cover the largest local KV shard].  Same
  * arguments, results and errors as dcp_mla_decode_partial, except:
  *
- *   block_table     int32 [D, B, bt_width]: shard d's j-th local token of
- *                   request b lives in cache row
- *                   table[d, b, j / block_size] * block_size + j % block_size.
+ *   shard_begin, shard_count
+ *                   the shards this call computes, [shard_begin, shard_begin +
+ *                   shard_count) of D (0 <= shard_begin, 1 <= shard_count,
+ *                   shard_begin + shard_count <= D, else DCP_ERR_INVALID_ARG):
+ *                   all D when one GPU holds every shard, one per DCP rank
+ *                   when each rank holds only its own.  D and interleave
+ *                   still define which tokens each shard owns.
+ *   O_part, lse_part
+ *                   fp32 [shard_count, T, H, 512] and [shard_count, T, H].
+ *   block_table     int32 [shard_count, B, bt_width]: shard d's j-th local
+ *                   token of request b lives in cache row
+ *                   table[d - shard_begin, b, j / block_size] * block_size +
+ *                   j % block_size.
  *                   Request rows are bt_stride elements apart (>= bt_width),
- *                   shard tables bt_shard_stride apart
- *                   (>= (B - 1) * bt_stride + bt_width, else
+ *                   shard tables bt_shard_stride apart (with more than one
+ *                   shard >= (B - 1) * bt_stride + bt_width, else
  *                   DCP_ERR_INVALID_ARG).  Only the columns a shard's local
  *                   tokens reach are read.
- *   bt_width        must cover the largest local shard (shard 0):
- *                   ceil(local_len(max_seq_len, 0, D, interleave) /
+ *   bt_width        must cover the largest computed local shard, the first:
+ *                   ceil(local_len(max_seq_len, shard_begin, D, interleave) /
  *                   block_size) <= bt_width, else DCP_ERR_TABLE_TOO_NARROW.
  *
  * The shard of a token and its local index follow the same interleave rule
  * (dcp_shard_of, dcp_local_len).  The workspace is sized by
- * dcp_decode_workspace_size as for the global layout.
+ * dcp_decode_workspace_size with its D argument = shard_count.
  */
 dcp_status_t dcp_mla_decode_partial_local(
     const void* q, int64_t q_stride_tok,
@@ -247,7 +257,7 @@ dcp_status_t dcp_mla_decode_partial_local(
     const int32_t* block_table, int32_t bt_width, int64_t bt_stride, int64_t bt_shard_stride,
     const int32_t* seq_lens, const int32_t* query_start_loc,
     int32_t B, int32_t T, int32_t H, int32_t max_seq_len, int32_t max_q_len,
-    int32_t D, int32_t interleave, float scale,
+    int32_t D, int32_t interleave, int32_t shard_begin, int32_t shard_count, float scale,
     float* O_part, float* lse_part,
     void* workspace, size_t workspace_bytes,
     int32_t* dev_error, void* stream);

@@ -56,8 +56,8 @@ EXPORTS = [
       _P, _P, _P, _SZ, _P, _P]),
     ("dcp_lse_combine", ctypes.c_int, [_P, _P, _P, _P, _I32, _I32, _I32, _I32, _P, ctypes.c_int, _P, _P]),
     ("dcp_mla_decode_partial_local", ctypes.c_int,
-     [_P, _I64, _P, _I32, _I32, _P, _I32, _I64, _I64, _P, _P, _I32, _I32, _I32, _I32, _I32, _I32, _I32, _F,
-      _P, _P, _P, _SZ, _P, _P]),
+     [_P, _I64, _P, _I32, _I32, _P, _I32, _I64, _I64, _P, _P, _I32, _I32, _I32, _I32, _I32, _I32, _I32, _I32,
+      _I32, _F, _P, _P, _P, _SZ, _P, _P]),
     ("dcp_decode_concat_cache", ctypes.c_int,
      [_P, _I64, _I64, _P, _I64, _I64, _P, _I64, _P, _I64, _P, _I32, _I32, _P, _I64, _P, _I64, _P, _P]),
     ("dcp_mla_decode_partial_noalloc", ctypes.c_int,
@@ -262,13 +262,18 @@ def dcp_mla_decode_partial(q, kv_cache, block_table, seq_lens, query_start_loc, 
 
 def dcp_mla_decode_partial_local(q, kv_cache, block_table, seq_lens, query_start_loc, O_part, lse_part, *,
                                  D: int, interleave: int, scale: float, max_seq_len: int, max_q_len: int,
+                                 shard_begin: int = 0, shard_count: Optional[int] = None,
                                  workspace: Optional[torch.Tensor] = None,
                                  dev_error: Optional[torch.Tensor] = None, stream=None) -> None:
-    """dcp_mla_decode_partial over per-shard tables: block_table int32
-    [D, B, W], shard d's j-th local token of request b in row
-    block_table[d, b, j // bs] * bs + j % bs."""
-    B, T, H = _decode_geometry(q, kv_cache, block_table, seq_lens, query_start_loc, O_part, lse_part, D,
-                               local=True)
+    """dcp_mla_decode_partial over per-shard tables for shards [shard_begin,
+    shard_begin + shard_count) of D (default all): block_table int32
+    [shard_count, B, W], shard d's j-th local token of request b in row
+    block_table[d - shard_begin, b, j // bs] * bs + j % bs; O_part and
+    lse_part have shard_count rows."""
+    if shard_count is None:
+        shard_count = D - shard_begin
+    B, T, H = _decode_geometry(q, kv_cache, block_table, seq_lens, query_start_loc, O_part, lse_part,
+                               shard_count, local=True)
     _need_opt(workspace, "workspace", allow_empty=True)
     if workspace is not None and workspace.numel() == 0:
         workspace = None
@@ -278,8 +283,8 @@ def dcp_mla_decode_partial_local(q, kv_cache, block_table, seq_lens, query_start
         st = lib().dcp_mla_decode_partial_local(
             _ptr(q), q.stride(0), _ptr(kv_cache), kv_cache.shape[0], kv_cache.shape[1], _ptr(block_table),
             block_table.shape[2], block_table.stride(1), block_table.stride(0), _ptr(seq_lens),
-            _ptr(query_start_loc), B, T, H, max_seq_len, max_q_len, D, interleave, scale, _ptr(O_part),
-            _ptr(lse_part), _ptr(workspace), ws_bytes, _ptr(dev_error), _stream(stream))
+            _ptr(query_start_loc), B, T, H, max_seq_len, max_q_len, D, interleave, shard_begin, shard_count,
+            scale, _ptr(O_part), _ptr(lse_part), _ptr(workspace), ws_bytes, _ptr(dev_error), _stream(stream))
     _check(st, "dcp_mla_decode_partial_local")
 
 

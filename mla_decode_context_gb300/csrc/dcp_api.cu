@@ -45,11 +45,12 @@ static int64_t split_cap(int32_t T, int32_t D, int64_t lmax, int sm_count) {
 }
 
 // Split-KV plan: pure function of its arguments (and the SM count).
-SplitPlan plan_splits(int32_t T, int32_t D, int32_t I, int32_t max_seq_len, int sm_count) {
+SplitPlan plan_splits(int32_t T, int32_t D, int32_t I, int32_t d0, int32_t Dn, int32_t max_seq_len, int sm_count) {
   SplitPlan p{1, kSplitRound};
-  const int32_t lmax = local_len(max_seq_len < 0 ? 0 : max_seq_len, 0, D, I);  // shard 0 is the largest
+  // the first computed shard is the largest of them
+  const int32_t lmax = local_len(max_seq_len < 0 ? 0 : max_seq_len, d0, D, I);
   if (lmax <= 0) return p;
-  const int64_t want = split_cap(T, D, lmax, sm_count);
+  const int64_t want = split_cap(T, Dn, lmax, sm_count);
   int64_t chunk = (lmax + want - 1) / want;
   chunk = (chunk + kSplitRound - 1) / kSplitRound * kSplitRound;
   p.chunk = static_cast<int32_t>(chunk);
@@ -89,19 +90,19 @@ struct DecodeLaunch {
   bool use_order;    // units start longest first (order kernel launched)
 };
 
-DecodeLaunch decode_launch(int32_t T, int32_t H, int32_t D, int32_t interleave, int32_t max_seq_len,
-                           bool have_workspace, size_t workspace_bytes) {
+DecodeLaunch decode_launch(int32_t T, int32_t H, int32_t D, int32_t interleave, int32_t d0, int32_t Dn,
+                           int32_t max_seq_len, bool have_workspace, size_t workspace_bytes) {
   DecodeLaunch L{};
   const int sms = dcp::current_sm_count();
-  L.plan = dcp::plan_splits(T, D, interleave, max_seq_len, sms);
-  L.need = dcp::split_workspace_bytes(L.plan, T, H, D);
-  L.obytes = dcp::order_workspace_bytes(L.plan, T, D);
+  L.plan = dcp::plan_splits(T, D, interleave, d0, Dn, max_seq_len, sms);
+  L.need = dcp::split_workspace_bytes(L.plan, T, H, Dn);
+  L.obytes = dcp::order_workspace_bytes(L.plan, T, Dn);
   dcp::DecodeArgs a{};
   a.H = H;
   a.plan = L.plan;
   const char* force = std::getenv("DCP_FORCE_SIMT");  // 1: the CUDA-core reference kernel (A/B checks)
   L.simt = (force && force[0] == '1') || !dcp::decode_tc_supported(a);
-  const int64_t units = static_cast<int64_t>(T) * D * L.plan.splits;
+  const int64_t units = static_cast<int64_t>(T) * Dn * L.plan.splits;
   const int resident = dcp::decode_tc_resident_ctas();  // 0: no device to size against
   L.use_order = !L.simt && resident > 0 && units > resident / 2 && have_workspace &&
                 workspace_bytes >= L.need + L.obytes;
@@ -154,6 +155,7 @@ size_t dcp_decode_workspace_size(int32_t B, int32_t T, int32_t H, int32_t D, int
 static dcp_status_t decode_partial_impl(const void* q, int64_t q_stride_tok, const void* kv_cache,
                                         int32_t num_blocks, int32_t block_size, const int32_t* block_table,
                                         int32_t bt_width, int64_t bt_stride, bool local, int64_t bt_shard_stride,
+                                        int32_t d0, int32_t Dn,
                                         const int32_t* seq_lens, const int32_t* query_start_loc, int32_t B,
                                         int32_t T, int32_t H, int32_t max_seq_len, int32_t max_q_len, int32_t D,
                                         int32_t interleave, float scale, float* O_part, float* lse_part,
@@ -169,15 +171,16 @@ static dcp_status_t decode_partial_impl(const void* q, int64_t q_stride_tok, con
     return DCP_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(kv_cache) || !aligned16(O_part) || (q_stride_tok % 8) != 0)
     return DCP_ERR_MISALIGNED;
-  if (local && bt_shard_stride < static_cast<int64_t>(B - 1) * bt_stride + bt_width)
+  if (d0 < 0 || Dn < 1 || d0 + Dn > D) return DCP_ERR_INVALID_ARG;
+  if (local && Dn > 1 && bt_shard_stride < static_cast<int64_t>(B - 1) * bt_stride + bt_width)
     return DCP_ERR_INVALID_ARG;  // shards' tables would overlap
   // a table row covers the longest sequence (global layout) or the largest
-  // local shard, shard 0 (per-shard layout)
-  const int64_t covered = local ? dcp::local_len(max_seq_len, 0, D, interleave) : max_seq_len;
+  // computed local shard, the first (per-shard layout)
+  const int64_t covered = local ? dcp::local_len(max_seq_len, d0, D, interleave) : max_seq_len;
   if ((covered + block_size - 1) / block_size > bt_width) return DCP_ERR_TABLE_TOO_NARROW;
 
   const DecodeLaunch launch =
-      decode_launch(T, H, D, interleave, max_seq_len, workspace != nullptr, workspace_bytes);
+      decode_launch(T, H, D, interleave, d0, Dn, max_seq_len, workspace != nullptr, workspace_bytes);
   const dcp::SplitPlan plan = launch.plan;
   const size_t need = launch.need;
   if (need > 0 && (workspace_bytes < need || !workspace)) return DCP_ERR_WORKSPACE_TOO_SMALL;
@@ -200,6 +203,7 @@ static dcp_status_t decode_partial_impl(const void* q, int64_t q_stride_tok, con
   a.B = B; a.T = T; a.H = H;
   a.max_seq_len = max_seq_len; a.max_q_len = max_q_len;
   a.D = D; a.I = interleave;
+  a.d0 = d0; a.Dn = Dn;
   a.scale = scale;
   a.plan = plan;
   a.dev_error = dev_error;
@@ -208,7 +212,7 @@ static dcp_status_t decode_partial_impl(const void* q, int64_t q_stride_tok, con
   float* ws_O = nullptr;
   float* ws_lse = nullptr;
   if (plan.splits > 1) {
-    const size_t pairs = static_cast<size_t>(plan.splits) * D * T * H;
+    const size_t pairs = static_cast<size_t>(plan.splits) * Dn * T * H;
     ws_O = static_cast<float*>(workspace);
     ws_lse = reinterpret_cast<float*>(static_cast<char*>(workspace) +
                                       (pairs * DCP_LATENT_DIM * sizeof(float) + 255) / 256 * 256);
@@ -225,7 +229,7 @@ static dcp_status_t decode_partial_impl(const void* q, int64_t q_stride_tok, con
     // more units than clusters that fit at once: start the long ones first
     // (the order lives in the workspace past the split partials; a workspace
     // without room for it keeps index order)
-    const int64_t units = static_cast<int64_t>(T) * D * plan.splits;
+    const int64_t units = static_cast<int64_t>(T) * Dn * plan.splits;
     int32_t* order = reinterpret_cast<int32_t*>(static_cast<char*>(workspace) + need);
     e = dcp::launch_unit_order(a, static_cast<int32_t>(units), order, st);
     if (e != cudaSuccess) return DCP_ERR_CUDA;
@@ -234,7 +238,7 @@ static dcp_status_t decode_partial_impl(const void* q, int64_t q_stride_tok, con
   e = simt ? dcp::launch_decode_simt(a, st) : dcp::launch_decode_tc(a, st);
   if (e != cudaSuccess) return DCP_ERR_CUDA;
   if (plan.splits > 1) {
-    const int64_t pairs = static_cast<int64_t>(D) * T * H;
+    const int64_t pairs = static_cast<int64_t>(Dn) * T * H;
     e = dcp::launch_lse_merge_f32(ws_O, ws_lse, pairs * DCP_LATENT_DIM, pairs, plan.splits, pairs, H,
                                   nullptr, nullptr, 0, /*row_mask=*/false, O_part, lse_part, st);
     if (e != cudaSuccess) return DCP_ERR_CUDA;
@@ -253,8 +257,8 @@ dcp_status_t dcp_mla_decode_partial(const void* q, int64_t q_stride_tok, const v
                                     float scale, float* O_part, float* lse_part, void* workspace,
                                     size_t workspace_bytes, int32_t* dev_error, void* stream) {
   return decode_partial_impl(q, q_stride_tok, kv_cache, num_blocks, block_size, block_table, bt_width, bt_stride,
-                             false, 0, seq_lens, query_start_loc, B, T, H, max_seq_len, max_q_len, D, interleave,
-                             scale, O_part, lse_part, workspace, workspace_bytes, dev_error, stream);
+                             false, 0, 0, D, seq_lens, query_start_loc, B, T, H, max_seq_len, max_q_len, D,
+                             interleave, scale, O_part, lse_part, workspace, workspace_bytes, dev_error, stream);
 }
 
 dcp_status_t dcp_mla_decode_partial_local(const void* q, int64_t q_stride_tok, const void* kv_cache,
@@ -262,12 +266,13 @@ dcp_status_t dcp_mla_decode_partial_local(const void* q, int64_t q_stride_tok, c
                                           int32_t bt_width, int64_t bt_stride, int64_t bt_shard_stride,
                                           const int32_t* seq_lens, const int32_t* query_start_loc, int32_t B,
                                           int32_t T, int32_t H, int32_t max_seq_len, int32_t max_q_len, int32_t D,
-                                          int32_t interleave, float scale, float* O_part, float* lse_part,
-                                          void* workspace, size_t workspace_bytes, int32_t* dev_error,
-                                          void* stream) {
+                                          int32_t interleave, int32_t shard_begin, int32_t shard_count,
+                                          float scale, float* O_part, float* lse_part, void* workspace,
+                                          size_t workspace_bytes, int32_t* dev_error, void* stream) {
   return decode_partial_impl(q, q_stride_tok, kv_cache, num_blocks, block_size, block_table, bt_width, bt_stride,
-                             true, bt_shard_stride, seq_lens, query_start_loc, B, T, H, max_seq_len, max_q_len, D,
-                             interleave, scale, O_part, lse_part, workspace, workspace_bytes, dev_error, stream);
+                             true, bt_shard_stride, shard_begin, shard_count, seq_lens, query_start_loc, B, T, H,
+                             max_seq_len, max_q_len, D, interleave, scale, O_part, lse_part, workspace,
+                             workspace_bytes, dev_error, stream);
 }
 
 int32_t dcp_decode_kernel_launches(int32_t B, int32_t T, int32_t H, int32_t D, int32_t interleave,
@@ -276,7 +281,8 @@ int32_t dcp_decode_kernel_launches(int32_t B, int32_t T, int32_t H, int32_t D, i
       max_q_len < 0)
     return -1;
   if (B == 0 || T == 0) return 0;
-  const DecodeLaunch L = decode_launch(T, H, D, interleave, max_seq_len, workspace_bytes > 0, workspace_bytes);
+  const DecodeLaunch L =
+      decode_launch(T, H, D, interleave, 0, D, max_seq_len, workspace_bytes > 0, workspace_bytes);
   return 1 + (L.plan.splits > 1 ? 1 : 0) + (L.use_order ? 1 : 0);
 }
 

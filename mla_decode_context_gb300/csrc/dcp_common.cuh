@@ -121,6 +121,7 @@ struct SplitPlan {
   int32_t chunk;
 };
 
-SplitPlan plan_splits(int32_t T, int32_t D, int32_t I, int32_t max_seq_len, int sm_count);
+// D, I: the interleave rule; [d0, d0 + Dn): the shards computed.
+SplitPlan plan_splits(int32_t T, int32_t D, int32_t I, int32_t d0, int32_t Dn, int32_t max_seq_len, int sm_count);
 
 }  // namespace dcp

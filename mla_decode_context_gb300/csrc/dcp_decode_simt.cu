@@ -41,11 +41,11 @@ decode_simt_kernel(DecodeArgs a) {
   const int hg = blockIdx.x % groups;
   const int r = blockIdx.x / groups;
   const int h = hg * kHeadsPerCta + warp;
-  const int d = blockIdx.y / a.plan.splits;
+  const int d = a.d0 + static_cast<int>(blockIdx.y) / a.plan.splits;  // shard (of D)
   const int s = blockIdx.y % a.plan.splits;
   const bool head_ok = h < a.H;
 
-  const int64_t dst_pair = ((static_cast<int64_t>(s) * a.D + d) * a.T + r) * a.H + h;
+  const int64_t dst_pair = ((static_cast<int64_t>(s) * a.Dn + (d - a.d0)) * a.T + r) * a.H + h;
   float* O_out = a.O_dst + dst_pair * kLatent;
 
   const RowInfo ri = resolve_row(a.seq_lens, a.qsl, a.B, r, a.max_seq_len, a.max_q_len);
@@ -73,7 +73,7 @@ decode_simt_kernel(DecodeArgs a) {
     }
     const float sl2 = a.scale * kLog2e;
     const int32_t* trow = a.block_table + static_cast<int64_t>(ri.b) * a.bt_stride +
-                          (a.local_tables ? static_cast<int64_t>(d) * a.bt_shard_stride : 0);
+                          (a.local_tables ? static_cast<int64_t>(d - a.d0) * a.bt_shard_stride : 0);
 
     for (int32_t t0 = lo; t0 < hi; t0 += kTile) {
       __syncthreads();  // previous tile fully consumed (and q staged)
@@ -184,7 +184,7 @@ cudaError_t launch_decode_simt(const DecodeArgs& a, cudaStream_t st) {
     }
   }
   const int64_t gx = static_cast<int64_t>((a.H + kHeadsPerCta - 1) / kHeadsPerCta) * a.T;
-  const int64_t gy = static_cast<int64_t>(a.D) * a.plan.splits;
+  const int64_t gy = static_cast<int64_t>(a.Dn) * a.plan.splits;
   if (gx > 0x7fffffffLL || gy > 65535) return cudaErrorInvalidConfiguration;
   const dim3 grid(static_cast<unsigned>(gx), static_cast<unsigned>(gy));
   decode_simt_kernel<<<grid, kThreads, smem, st>>>(a);

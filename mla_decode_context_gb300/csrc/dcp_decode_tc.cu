@@ -255,18 +255,18 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(DecodeArgs a) {
   const uint32_t peer = cta ^ 1u;
 
   const int64_t unit = a.unit_order ? __ldg(a.unit_order + (blockIdx.x >> 1)) : (blockIdx.x >> 1);
-  const int per_row = a.D * a.plan.splits;
+  const int per_row = a.Dn * a.plan.splits;
   const int r = static_cast<int>(unit / per_row);
-  const int d = static_cast<int>((unit % per_row) / a.plan.splits);
+  const int d = a.d0 + static_cast<int>((unit % per_row) / a.plan.splits);  // shard (of D)
   const int s = static_cast<int>(unit % a.plan.splits);
 
   const RowInfo ri = resolve_row(a.seq_lens, a.qsl, a.B, r, a.max_seq_len, a.max_q_len);
-  if (ri.err && threadIdx.x == 0 && cta == 0 && d == 0 && s == 0) report(a.dev_error, ri.err);
+  if (ri.err && threadIdx.x == 0 && cta == 0 && d == a.d0 && s == 0) report(a.dev_error, ri.err);
   const int32_t n_local = ri.padding ? 0 : local_len(ri.L, d, a.D, a.I);
   const int32_t lo = s * a.plan.chunk;
   const int32_t hi = min(n_local, lo + a.plan.chunk);
   const int ntiles = lo < hi ? (hi - lo + kTile - 1) / kTile : 0;
-  const int64_t pair0 = ((static_cast<int64_t>(s) * a.D + d) * a.T + r) * a.H;
+  const int64_t pair0 = ((static_cast<int64_t>(s) * a.Dn + (d - a.d0)) * a.T + r) * a.H;
 
   if (ntiles == 0) {
     // empty shard / split or padding row: masked at the source, no KV read
@@ -377,7 +377,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(DecodeArgs a) {
 
   // the request's table row (global layout) or this shard's row of it (per-shard layout)
   const int32_t* trow = a.block_table + static_cast<int64_t>(ri.b) * a.bt_stride +
-                        (a.local_tables ? static_cast<int64_t>(d) * a.bt_shard_stride : 0);
+                        (a.local_tables ? static_cast<int64_t>(d - a.d0) * a.bt_shard_stride : 0);
   const uint32_t smem_base = smem_u32(smem);
   int pdone = 0;  // value, warps 0-3: P tiles received
 
@@ -961,8 +961,8 @@ __global__ void __launch_bounds__(1024) unit_order_kernel(DecodeArgs a, int32_t 
   __shared__ int32_t wcnt[32][33];
   const int t = threadIdx.x, w = t >> 5, lane = t & 31;
   auto key_of = [&](int32_t u) -> int {
-    const int per_row = a.D * a.plan.splits;
-    const int r = u / per_row, d = (u % per_row) / a.plan.splits, s = u % a.plan.splits;
+    const int per_row = a.Dn * a.plan.splits;
+    const int r = u / per_row, d = a.d0 + (u % per_row) / a.plan.splits, s = u % a.plan.splits;
     const RowInfo ri = resolve_row(a.seq_lens, a.qsl, a.B, r, a.max_seq_len, a.max_q_len);
     const int32_t n = ri.padding ? 0 : local_len(ri.L, d, a.D, a.I);
     const int32_t lo = s * a.plan.chunk, hi = min(n, lo + a.plan.chunk);
@@ -1083,7 +1083,7 @@ extern "C" int dcp_timeline_fetch(void* dst, size_t bytes) {
 cudaError_t launch_decode_tc(const DecodeArgs& a, cudaStream_t st) {
   if (!decode_tc_supported(a)) return cudaErrorInvalidValue;
   if (setup_current_device() <= 0) return cudaErrorInvalidDevice;
-  const int64_t units = static_cast<int64_t>(a.T) * a.D * a.plan.splits;
+  const int64_t units = static_cast<int64_t>(a.T) * a.Dn * a.plan.splits;
   if (2 * units > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
   cudaLaunchAttribute attr[1];
   cudaLaunchConfig_t cfg = launch_config(units, st, attr);

@@ -27,9 +27,13 @@ struct DecodeArgs {
   const int32_t* seq_lens;
   const int32_t* qsl;
   int32_t B, T, H, max_seq_len, max_q_len, D, I;
+  // the shards this launch computes: d0 .. d0 + Dn - 1 (all D on one GPU;
+  // one per rank when each DCP rank holds only its own shard).  Outputs and
+  // per-shard tables are indexed by d - d0.
+  int32_t d0, Dn;
   float scale;
-  // Where partials go: O_dst[((s * D + d) * T + r) * H + h][512] with s the
-  // split (s == 0 only when splits == 1, then O_dst = O_part).
+  // Where partials go: O_dst[((s * Dn + d - d0) * T + r) * H + h][512] with s
+  // the split (s == 0 only when splits == 1, then O_dst = O_part).
   float* O_dst;
   float* lse_dst;
   SplitPlan plan;

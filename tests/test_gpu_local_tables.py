@@ -87,3 +87,29 @@ def test_local_table_must_cover_the_largest_shard():
 @pytest.mark.parametrize("spec", [wl.LONG_120K_B2_PREFIX, wl.LONG_120K_B2_PREFIX_LOCAL], ids=lambda s: s.name)
 def test_long_context_shared_prefix_b2(spec):
     _check(wl.make_decode_inputs(spec))
+
+
+@pytest.mark.parametrize("spec", [LOCAL[0], LOCAL[3]], ids=lambda s: s.name)
+def test_one_shard_per_call_as_a_rank_would(spec, kernel):
+    """Each DCP rank computes only its own shard: calls over shard d alone
+    (its table, shard_begin = d, shard_count = 1) reproduce the oracle's
+    shard-d partials."""
+    import mla_decode_context_gb300 as dcp
+    inp = wl.make_decode_inputs(spec)
+    t = G.to_device(inp)
+    O_ref, lse_ref, rows = oracle.decode_partial(inp)
+    D, T, H = inp["D"], inp["T"], inp["H"]
+    msl, mql = max(1, inp["max_seq_len"]), max(1, inp["max_q_len"])
+    for d in range(D):
+        O = torch.empty((1, T, H, 512), device="cuda")
+        lse = torch.empty((1, T, H), device="cuda")
+        ws = dcp.decode_workspace(inp["B"], T, H, 1, msl, mql)
+        err = torch.zeros(1, dtype=torch.int32, device="cuda")
+        dcp.dcp_mla_decode_partial_local(t["q"], t["kv_cache"], t["block_table"][d:d + 1], t["seq_lens"],
+                                         t["query_start_loc"], O, lse, D=D, interleave=inp["interleave"],
+                                         scale=inp["scale"], max_seq_len=msl, max_q_len=mql, shard_begin=d,
+                                         shard_count=1, workspace=ws, dev_error=err)
+        torch.cuda.synchronize()
+        assert int(err.item()) == 0
+        G.check_partials(O.cpu().numpy(), lse.cpu().numpy(), O_ref[d:d + 1], lse_ref[d:d + 1],
+                         "%s shard %d" % (spec.name, d))
