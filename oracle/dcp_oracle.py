@@ -51,6 +51,7 @@ __all__ = [
     "bf16_to_f64", "row_lengths", "shard_of", "local_len", "shard_positions",
     "physical_rows", "physical_rows_local", "gather_latents", "scores", "shard_partial",
     "decode_partial_row", "decode_partial", "lse_combine", "attention", "concat_cache",
+    "fp8_e4m3_to_f64", "kv_rows_f64",
 ]
 
 
@@ -187,10 +188,12 @@ def shard_partial(s: np.ndarray, values: np.ndarray):
 
 def decode_partial_row(q_heads: np.ndarray, kv_cache_bits: np.ndarray, table_row: np.ndarray,
                        block_size: int, L: int, D: int, I: int, scale: float, padding: bool,
-                       local: bool = False):
+                       local: bool = False, rows_f64: np.ndarray = None):
     """(O [D, H, 512], lse [D, H]) of one query row over its own L tokens.
     table_row is the request's block-table row, or with ``local`` its D
     per-shard rows [D, W] (the shard's tokens gathered by local index).
+    ``rows_f64`` ([num_blocks * block_size, 576], from kv_rows_f64) replaces
+    the bf16 cache bits, e.g. for an fp8 cache.
 
     Empty shards and padding rows are masked at the source: lse = -inf,
     O = NaN [PR50484, Summary: empty-KV-shard masking; PRHUB, implementation
@@ -206,8 +209,13 @@ def decode_partial_row(q_heads: np.ndarray, kv_cache_bits: np.ndarray, table_row
         if pos.size == 0:
             continue
         if local:
-            nb, bs, kd = kv_cache_bits.shape
             rows = physical_rows_local(table_row[d], block_size, pos.size)
+        else:
+            rows = physical_rows(table_row, block_size, pos)
+        if rows_f64 is not None:
+            kv = rows_f64[rows]
+        elif local:
+            nb, bs, kd = kv_cache_bits.shape
             kv = bf16_to_f64(kv_cache_bits.reshape(nb * bs, kd)[rows])
         else:
             kv = gather_latents(kv_cache_bits, table_row, block_size, pos)
@@ -225,6 +233,8 @@ def decode_partial(inp: dict, rows=None):
     """
     T, H, D = inp["T"], inp["H"], inp["D"]
     local = inp.get("layout", "global") == "local"
+    fp8 = inp.get("kv_dtype", "bf16") == "fp8_e4m3"
+    rows_f64 = kv_rows_f64(inp) if fp8 else None
     req, L, padding = row_lengths(inp["seq_lens"], inp["query_start_loc"], T)
     rows = np.arange(T) if rows is None else np.asarray(rows, dtype=np.int64)
     O = np.full((D, len(rows), H, LATENT), np.nan)
@@ -237,7 +247,7 @@ def decode_partial(inp: dict, rows=None):
             table_row = inp["block_table"][:, b] if local else inp["block_table"][b]
         O[:, j], lse[:, j] = decode_partial_row(
             inp["q"][r], inp["kv_cache"], table_row, inp["block_size"], int(L[r]),
-            D, inp["interleave"], inp["scale"], bool(padding[r]), local=local)
+            D, inp["interleave"], inp["scale"], bool(padding[r]), local=local, rows_f64=rows_f64)
     return O, lse, rows
 
 
@@ -322,3 +332,35 @@ def concat_cache(ql_nope: np.ndarray, q_pe: np.ndarray, kv_c: np.ndarray, k_pe: 
         flat[slot, :LATENT] = kv_c[t]
         flat[slot, LATENT:] = k_pe[t]
     return q, cache
+
+
+# ---------------------------------------------------------------------------
+# fp8 latent KV cache (per-token scale)
+# ---------------------------------------------------------------------------
+def fp8_e4m3_to_f64(codes: np.ndarray) -> np.ndarray:
+    """Widen FP8 E4M3 codes (uint8: 1 sign bit, 4 exponent bits with bias 7,
+    3 mantissa bits; exponent 0 is subnormal, 0x7F / 0xFF are NaN, there is no
+    infinity) exactly to float64, from the format's definition: a normal code
+    is (-1)^s * 2^(e - 7) * (1 + m / 8), a subnormal one (-1)^s * 2^-6 * m / 8.
+    [the fp8 KV verify plans of "perf(mla): fuse K3 DCP verification
+    queries", review follow-up, store latent KV in this 8-bit format]."""
+    c = np.asarray(codes, dtype=np.uint8).astype(np.int64)
+    s = np.where(c >> 7, -1.0, 1.0)
+    e = (c >> 3) & 0xF
+    m = c & 0x7
+    mag = np.where(e == 0, np.ldexp(m / 8.0, -6), np.ldexp(1.0 + m / 8.0, e - 7))
+    out = s * mag
+    return np.where((c & 0x7F) == 0x7F, np.nan, out)
+
+
+def kv_rows_f64(inp: dict) -> np.ndarray:
+    """All cache rows widened to float64 [num_blocks * block_size, 576]: bf16
+    bits, or fp8 E4M3 codes times the slot's fp32 scale when the cache is
+    fp8 (``inp["kv_dtype"] == "fp8_e4m3"``, scales in ``inp["kv_scale"]``
+    [num_blocks, block_size])."""
+    kv = inp["kv_cache"]
+    nb, bs, kd = kv.shape
+    if inp.get("kv_dtype", "bf16") == "fp8_e4m3":
+        scale = np.asarray(inp["kv_scale"], dtype=np.float32).astype(np.float64).reshape(nb * bs, 1)
+        return fp8_e4m3_to_f64(kv.reshape(nb * bs, kd)) * scale
+    return bf16_to_f64(kv.reshape(nb * bs, kd))

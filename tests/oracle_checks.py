@@ -386,3 +386,62 @@ def check_shared_prefix(o):
     # the suffixes differ
     assert not np.array_equal(o.gather_latents(inp["kv_cache"], t[0], 16, np.arange(96, 150)),
                               o.gather_latents(inp["kv_cache"], t[1], 16, np.arange(96, 150)))
+
+
+# ---------------------------------------------------------------------------
+# fp8 latent KV
+# ---------------------------------------------------------------------------
+def fp8_table() -> dict:
+    out = {}
+    with open(os.path.join(GOLDEN, "fp8_e4m3_table.txt")) as f:
+        for line in f:
+            line = line.split("|")[0].strip()
+            if not line or line.startswith("#"):
+                continue
+            k, v = (x.strip() for x in line.split("="))
+            out[int(k, 16)] = float(v)
+    return out
+
+
+def check_fp8_widening(o):
+    """The hand-decoded E4M3 table, and every one of the 256 codes against
+    torch's float8_e4m3fn -> float conversion (NaN codes alike)."""
+    tab = fp8_table()
+    codes = np.array(sorted(tab), dtype=np.uint8)
+    got = o.fp8_e4m3_to_f64(codes)
+    want = np.array([tab[c] for c in sorted(tab)])
+    assert np.array_equal(np.isnan(got), np.isnan(want))
+    ok = ~np.isnan(want)
+    assert np.array_equal(got[ok], want[ok]) and np.array_equal(np.signbit(got[ok]), np.signbit(want[ok]))
+    allc = np.arange(256, dtype=np.uint8)
+    ref = torch.from_numpy(allc).view(torch.float8_e4m3fn).double().numpy()
+    g = o.fp8_e4m3_to_f64(allc)
+    assert np.array_equal(np.isnan(g), np.isnan(ref))
+    assert np.array_equal(g[~np.isnan(g)], ref[~np.isnan(ref)])
+
+
+def check_fp8_decode_matches_bf16_twin(o):
+    """An fp8 cache with power-of-two per-token scales holds values that bf16
+    represents exactly; the oracle's decode over the fp8 cache equals its
+    decode over the bf16 cache of the same values (the fp8 path changes only
+    the storage)."""
+    import workloads as wl
+    spec = wl.DecodeSpec("f8", seed=131, B=3, seq_lens=(70, 5, 0), q_len=2, H=3, block_size=16, D=4, interleave=2,
+                         kv_dtype="fp8_e4m3")
+    f = wl.make_decode_inputs(spec)
+    # the twin's values come from torch's own E4M3 conversion times the stored
+    # per-slot scale, independently of the oracle's widening
+    nb, bs, kd = f["kv_cache"].shape
+    codes = torch.from_numpy(f["kv_cache"].reshape(nb * bs, kd)).view(torch.float8_e4m3fn).double()
+    vals = (codes * torch.from_numpy(f["kv_scale"].reshape(nb * bs, 1)).double()).numpy()
+    live = ~np.isnan(vals).any(axis=1)
+    t32 = torch.from_numpy(vals[live].astype(np.float32))
+    assert torch.equal(t32.to(torch.bfloat16).float(), t32)  # exact in bf16
+    bits = np.full(vals.shape, 0x7FC0, dtype=np.uint16)
+    bits[live] = t32.to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    twin = dict(f, kv_dtype="bf16", kv_cache=bits.reshape(f["kv_cache"].shape), kv_scale=None)
+    Of, lf, _ = o.decode_partial(f)
+    Ob, lb, _ = o.decode_partial(twin)
+    assert np.array_equal(lf, lb)
+    m = ~np.isnan(Ob)
+    assert np.array_equal(np.isnan(Of), ~m) and np.array_equal(Of[m], Ob[m])

@@ -108,3 +108,11 @@ def test_local_layout_matches_global():
 
 def test_shared_prefix_blocks_and_values():
     C.check_shared_prefix(oracle)
+
+
+def test_fp8_e4m3_widening():
+    C.check_fp8_widening(oracle)
+
+
+def test_fp8_decode_matches_its_bf16_twin():
+    C.check_fp8_decode_matches_bf16_twin(oracle)

@@ -133,3 +133,20 @@ def test_local_walker_by_position_is_caught(monkeypatch):
         return blocks * block_size + j % block_size
     monkeypatch.setattr(O, "physical_rows_local", bad)
     _fails(C.check_local_layout_matches_global)
+
+
+def test_fp8_bias_8_is_caught(monkeypatch):
+    real = O.fp8_e4m3_to_f64
+    monkeypatch.setattr(O, "fp8_e4m3_to_f64", lambda c: real(c) / 2.0)  # exponent bias 8 instead of 7
+    _fails(C.check_fp8_widening)
+
+
+def test_fp8_scale_ignored_is_caught(monkeypatch):
+    def bad(inp):
+        kv = inp["kv_cache"]
+        nb, bs, kd = kv.shape
+        if inp.get("kv_dtype", "bf16") == "fp8_e4m3":
+            return O.fp8_e4m3_to_f64(kv.reshape(nb * bs, kd))
+        return O.bf16_to_f64(kv.reshape(nb * bs, kd))
+    monkeypatch.setattr(O, "kv_rows_f64", bad)
+    _fails(C.check_fp8_decode_matches_bf16_twin)

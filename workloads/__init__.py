@@ -43,9 +43,24 @@ ROPE = 64             # k_pe dims
 KDIM = LATENT + ROPE  # 576: the width of one latent cache row and of one query head row
 CHUNK = 2048          # tokens per independently seeded chunk
 BF16_NAN = np.uint16(0x7FC0)
+FP8_NAN = np.uint8(0x7F)   # FP8 E4M3 NaN code
 
 # stream tags for default_rng([seed, stream, ...])
 _S_SEQ, _S_TABLE, _S_KV, _S_KV_SUFFIX, _S_Q, _S_COMBINE = 0, 1, 2, 3, 4, 5
+
+
+def quantize_fp8_e4m3(x: np.ndarray):
+    """Per-row FP8 E4M3 codes and scales of float32 rows [n, 576]: scale =
+    2^ceil(log2(max |x| / 256)) (1 for an all-zero row), codes = x / scale
+    rounded to the nearest E4M3 value (ties to even; torch's conversion).
+    Power-of-two scales keep x / scale exact before the rounding."""
+    import torch
+    amax = np.abs(x).max(axis=1)
+    e = np.ceil(np.log2(np.where(amax > 0, amax / 256.0, 1.0)))
+    sc = np.ldexp(np.float32(1.0), e.astype(np.int32)).astype(np.float32)
+    y = torch.from_numpy(np.ascontiguousarray(x / sc[:, None], dtype=np.float32))
+    codes = y.to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    return codes, sc
 
 
 def f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:
@@ -82,6 +97,10 @@ class DecodeSpec:
     # the first prefix_len tokens of every request are the same tokens (drawn
     # once) stored in the same blocks (those holding only prefix tokens)
     shared_prefix: bool = False
+    # latent cache format: "bf16", or "fp8_e4m3" codes with one fp32 scale per
+    # cache slot (a power of two per token: 2^ceil(log2(max |x| / 256)), so
+    # that every code stays within the format's finite range)
+    kv_dtype: str = "bf16"
 
     def q_lens(self) -> Tuple[int, ...]:
         if isinstance(self.q_len, int):
@@ -131,8 +150,7 @@ def _threads() -> int:
     return max(1, min(32, os.cpu_count() or 1))
 
 
-def _fill_request(kv_flat: np.ndarray, phys_rows: np.ndarray, spec: DecodeSpec,
-                  b: int, L: int) -> None:
+def _fill_request(store, phys_rows: np.ndarray, spec: DecodeSpec, b: int, L: int) -> None:
     """Draw request b's L latent rows in logical order and store them.  With a
     shared prefix every request draws its prefix from request 0's stream."""
     jobs = []
@@ -148,7 +166,7 @@ def _fill_request(kv_flat: np.ndarray, phys_rows: np.ndarray, spec: DecodeSpec,
         stream, owner, c, start, stop = job
         rng = np.random.default_rng([spec.seed, stream, owner, c])
         x = rng.standard_normal((stop - start, KDIM), dtype=np.float32)
-        kv_flat[phys_rows[start:stop]] = f32_to_bf16_bits(x)
+        store(phys_rows[start:stop], x)
 
     if len(jobs) == 1:
         work(jobs[0])
@@ -180,12 +198,23 @@ def make_decode_inputs(spec: DecodeSpec, kv_rows=None) -> dict:
     placement = _place_global if spec.layout == "global" else _place_local
     table, phys_of, num_blocks = placement(spec, seq)
 
-    kv = np.empty((num_blocks, bs, KDIM), dtype=np.uint16)
+    fp8 = spec.kv_dtype == "fp8_e4m3"
+    kv = np.empty((num_blocks, bs, KDIM), dtype=np.uint8 if fp8 else np.uint16)
     if spec.tail_fill_nan:
-        kv.fill(BF16_NAN)
+        kv.fill(FP8_NAN if fp8 else BF16_NAN)
     else:
         kv.fill(0)
     kv_flat = kv.reshape(num_blocks * bs, KDIM)
+    kv_scale = np.ones((num_blocks, bs), dtype=np.float32) if fp8 else None
+
+    def store(rows, x):
+        if fp8:
+            codes, sc = quantize_fp8_e4m3(x)
+            kv_flat[rows] = codes
+            kv_scale.reshape(-1)[rows] = sc
+        else:
+            kv_flat[rows] = f32_to_bf16_bits(x)
+
     for b in range(B):
         L = int(seq[b])
         if L == 0:
@@ -193,9 +222,10 @@ def make_decode_inputs(spec: DecodeSpec, kv_rows=None) -> dict:
         pos = np.arange(L, dtype=np.int64)
         phys = phys_of(b, pos)
         if kv_rows is None:
-            _fill_request(kv_flat, phys, spec, b, L)
+            _fill_request(store, phys, spec, b, L)
         else:
-            kv_flat[phys] = kv_rows(b, pos)
+            bits = kv_rows(b, pos)
+            store(phys, (bits.astype(np.uint32) << np.uint32(16)).view(np.float32))
 
     q = f32_to_bf16_bits(np.random.default_rng([spec.seed, _S_Q]).standard_normal(
         (T, spec.H, KDIM), dtype=np.float32))
@@ -204,7 +234,7 @@ def make_decode_inputs(spec: DecodeSpec, kv_rows=None) -> dict:
         query_start_loc=qsl, B=B, T=T, H=spec.H, D=spec.D,
         interleave=spec.interleave, block_size=bs, scale=float(spec.scale),
         max_seq_len=int(seq.max(initial=0)), max_q_len=int(qlens.max(initial=0)),
-        num_blocks=num_blocks, layout=spec.layout,
+        num_blocks=num_blocks, layout=spec.layout, kv_dtype=spec.kv_dtype, kv_scale=kv_scale,
     )
 
 
@@ -351,8 +381,14 @@ def to_torch(inp: dict, device="cuda") -> dict:
 
     def bf16(bits):
         return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).to(device)
+    if inp.get("kv_dtype", "bf16") == "fp8_e4m3":
+        kv = torch.from_numpy(np.ascontiguousarray(inp["kv_cache"])).to(device)
+        extra = dict(kv_scale=torch.from_numpy(inp["kv_scale"]).to(device))
+    else:
+        kv = bf16(inp["kv_cache"])
+        extra = {}
     return dict(
-        q=bf16(inp["q"]), kv_cache=bf16(inp["kv_cache"]),
+        q=bf16(inp["q"]), kv_cache=kv, **extra,
         block_table=torch.from_numpy(inp["block_table"]).to(device),
         seq_lens=torch.from_numpy(inp["seq_lens"]).to(device),
         query_start_loc=torch.from_numpy(inp["query_start_loc"]).to(device),
