@@ -101,22 +101,25 @@ def kv_tokens(inp) -> int:
     return int(np.asarray(inp["seq_lens"], dtype=np.int64).sum())
 
 
-def decode_bytes(inp) -> int:
+def decode_bytes(inp, o_bytes: int = 4) -> int:
     """Algorithmic HBM bytes of one decode launch: each live KV latent row once
-    (1152 B), the query rows, and the partial outputs + LSEs written."""
+    (1152 B in bf16; 576 B of FP8 codes + a 4 B scale in fp8), the query rows,
+    and the partial outputs (o_bytes per element) + fp32 LSEs written."""
     T, H, D = inp["T"], inp["H"], inp["D"]
-    return kv_tokens(inp) * KV_ROW_BYTES + T * H * 576 * 2 + D * T * H * (512 + 1) * 4
+    row = 576 + 4 if inp.get("kv_dtype", "bf16") == "fp8_e4m3" else KV_ROW_BYTES
+    return kv_tokens(inp) * row + T * H * 576 * 2 + D * T * H * (512 * o_bytes + 4)
 
 
-def combine_bytes(inp, lse_part_host=None) -> int:
-    """Algorithmic bytes of one combine: live partials read (skipped empty and
-    padding pairs excluded), LSEs read, bf16 outputs + fp32 LSEs written."""
+def combine_bytes(inp, lse_part_host=None, o_bytes: int = 4) -> int:
+    """Algorithmic bytes of one combine: live partials read (o_bytes per
+    element; skipped empty and padding pairs excluded), LSEs read, bf16
+    outputs + fp32 LSEs written."""
     T, H, D = inp["T"], inp["H"], inp["D"]
     if lse_part_host is not None:
         live = int(np.isfinite(lse_part_host).sum())
     else:
         live = D * T * H
-    return live * 512 * 4 + D * T * H * 4 + T * H * (512 * 2 + 4)
+    return live * 512 * o_bytes + D * T * H * 4 + T * H * (512 * 2 + 4)
 
 
 class Clocks:
@@ -226,6 +229,8 @@ def workload_config(spec, inp, n_gpus: int) -> dict:
         cfg["block_tables"] = "per-shard (rank-local)"
     if spec.shared_prefix:
         cfg["shared_prefix"] = spec.prefix_len
+    if spec.kv_dtype != "bf16":
+        cfg["kv_cache"] = spec.kv_dtype
     return cfg
 
 
@@ -293,15 +298,17 @@ class DecodeBench:
     """One decode workload resident on the device, with its outputs,
     workspace and the two library calls of a step (decode, combine)."""
 
-    def __init__(self, spec, dev, use_graphs=True):
+    def __init__(self, spec, dev, use_graphs=True, o_dtype=None):
         import torch
         import mla_decode_context_gb300 as dcp
+        o_dtype = torch.float32 if o_dtype is None else o_dtype
         self.spec, self.dev = spec, dev
+        self.o_bytes = 2 if o_dtype == torch.bfloat16 else 4
         self.inp = inp = wl.make_decode_inputs(spec)
         self.t = t = wl.to_torch(inp, dev)
         D, T, H, I, B = inp["D"], inp["T"], inp["H"], inp["interleave"], inp["B"]
         self.msl, self.mql = msl, mql = max(1, inp["max_seq_len"]), max(1, inp["max_q_len"])
-        self.O = O = torch.empty((D, T, H, 512), dtype=torch.float32, device=dev)
+        self.O = O = torch.empty((D, T, H, 512), dtype=o_dtype, device=dev)
         self.lse = lse = torch.empty((D, T, H), dtype=torch.float32, device=dev)
         self.out = out = torch.empty((T, H, 512), dtype=torch.bfloat16, device=dev)
         self.out_lse = out_lse = torch.empty((T, H), dtype=torch.float32, device=dev)
@@ -311,10 +318,18 @@ class DecodeBench:
         self.launches = 1 + dcp.dcp_decode_kernel_launches(B, T, H, D, I, msl, mql,
                                                            work.numel() if work is not None else 0)
 
+        general = spec.kv_dtype != "bf16" or spec.layout != "global" or o_dtype != torch.float32
+
         def decode():
-            dcp.dcp_mla_decode_partial(t["q"], t["kv_cache"], t["block_table"], t["seq_lens"],
-                                       t["query_start_loc"], O, lse, D=D, interleave=I, scale=inp["scale"],
-                                       max_seq_len=msl, max_q_len=mql, workspace=work, dev_error=derr)
+            if general:  # fp8 cache, per-shard tables or bf16 partials
+                dcp.dcp_mla_decode_partial_v2(t["q"], t["kv_cache"], t["block_table"], t["seq_lens"],
+                                              t["query_start_loc"], O, lse, D=D, interleave=I, scale=inp["scale"],
+                                              max_seq_len=msl, max_q_len=mql, kv_scale=t.get("kv_scale"),
+                                              workspace=work, dev_error=derr)
+            else:
+                dcp.dcp_mla_decode_partial(t["q"], t["kv_cache"], t["block_table"], t["seq_lens"],
+                                           t["query_start_loc"], O, lse, D=D, interleave=I, scale=inp["scale"],
+                                           max_seq_len=msl, max_q_len=mql, workspace=work, dev_error=derr)
 
         def combine():
             dcp.dcp_lse_combine(O, lse, t["seq_lens"], t["query_start_loc"], out, out_lse)
@@ -372,7 +387,7 @@ class DecodeBench:
         inp = self.inp
         peak, peak_kind = peaks()
         tpeak, tpeak_kind = tensor_peak()
-        dbytes = decode_bytes(inp)
+        dbytes = decode_bytes(inp, self.o_bytes)
         dflops = decode_flops(inp)
         achieved = dbytes / (dec_ms * 1e-3) / 1e9
         tflops = dflops / (dec_ms * 1e-3) / 1e12
@@ -543,6 +558,19 @@ def run_gb300(args, spec):
                 "decode_ms_median": dmed, "combine_ms_median": float(np.median(c_ms)),
                 "kv_tokens_per_s": kv_tokens(ob.inp) / ((dmed + float(np.median(c_ms))) * 1e-3),
                 "roofline": ob.roofline(dmed), "gpu_launches_per_step": ob.launches}
+            ob.release()
+        for name, other, od in (("long_ctx_120k_b1_d8_i1 bf16 partials", wl.LONG_120K, torch.bfloat16),
+                                ("long_ctx_120k_b1_d8_i1 fp8 cache", wl.LONG_120K_FP8, None)):
+            ob = DecodeBench(other, dev, use_graphs=not args.eager, o_dtype=od)
+            d_ms, c_ms = ob.timed(max(5, min(args.steps, 20)), 3, flush)
+            dmed = float(np.median(d_ms))
+            cfg = workload_config(other, ob.inp, 1)
+            cfg["partials"] = "bf16" if od is not None else "fp32"
+            recs[name] = {
+                "config": cfg, "decode_ms_median": dmed, "combine_ms_median": float(np.median(c_ms)),
+                "kv_tokens_per_s": kv_tokens(ob.inp) / ((dmed + float(np.median(c_ms))) * 1e-3),
+                "roofline": ob.roofline(dmed), "gpu_launches_per_step": ob.launches,
+                "kernel": "CUDA cores (fp8 cache)" if other.kv_dtype != "bf16" else "tensor cores"}
             ob.release()
         recs["combine_sweep_h128"] = combine_sweep_record(dev, flush)
         res["workloads"] = recs

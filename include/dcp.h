@@ -88,6 +88,12 @@ typedef enum {
 
 typedef enum { DCP_DTYPE_BF16 = 0, DCP_DTYPE_F32 = 1 } dcp_dtype_t;
 
+/* Latent KV cache formats: bf16 rows, or FP8 E4M3 codes (1 sign, 4 exponent
+ * bits with bias 7, 3 mantissa bits; no infinity) with one fp32 scale per
+ * cache slot (value = code x scale) ["perf(mla): fuse K3 DCP verification
+ * queries", review follow-up: fp8 KV verify plans]. */
+typedef enum { DCP_KV_BF16 = 0, DCP_KV_FP8_E4M3 = 1 } dcp_kv_dtype_t;
+
 /* Human-readable name of a status code (static string, never NULL). */
 const char* dcp_status_str(dcp_status_t status);
 
@@ -261,6 +267,54 @@ dcp_status_t dcp_mla_decode_partial_local(
     float* O_part, float* lse_part,
     void* workspace, size_t workspace_bytes,
     int32_t* dev_error, void* stream);
+
+/*
+ * The general form of the decode: dcp_mla_decode_partial with every option.
+ * The fp8 latent cache and bf16 partials are the pages' next step for the
+ * hot path (they halve its two byte streams) ["perf(mla): fuse K3 DCP
+ * verification queries", review follow-up: fp8 KV verify plans].
+ *
+ *   kv_dtype        DCP_KV_BF16: kv_cache bf16 [num_blocks, block_size, 576].
+ *                   DCP_KV_FP8_E4M3: kv_cache uint8 codes [num_blocks,
+ *                   block_size, 576] and kv_scale fp32 [num_blocks,
+ *                   block_size] (required, else DCP_ERR_INVALID_ARG); the
+ *                   latent value of a slot is code x scale.  Other values:
+ *                   DCP_ERR_UNSUPPORTED_DTYPE.  The fp8 form runs on the
+ *                   CUDA-core kernel.
+ *   per_shard_tables, bt_shard_stride, shard_begin, shard_count
+ *                   0: one table row per request ([B, bt_width]); 1:
+ *                   per-shard tables as for dcp_mla_decode_partial_local.
+ *                   Either way the call computes shards [shard_begin,
+ *                   shard_begin + shard_count) of D.
+ *   O_part, o_dtype fp32 or bf16 (round to nearest even) [shard_count, T,
+ *                   H, 512]; lse_part stays fp32.  With bf16 the split-KV
+ *                   partials in the workspace are bf16 too.
+ * Everything else as for dcp_mla_decode_partial.
+ */
+dcp_status_t dcp_mla_decode_partial_v2(
+    const void* q, int64_t q_stride_tok,
+    const void* kv_cache, dcp_kv_dtype_t kv_dtype, const float* kv_scale,
+    int32_t num_blocks, int32_t block_size,
+    const int32_t* block_table, int32_t bt_width, int64_t bt_stride,
+    int32_t per_shard_tables, int64_t bt_shard_stride, int32_t shard_begin, int32_t shard_count,
+    const int32_t* seq_lens, const int32_t* query_start_loc,
+    int32_t B, int32_t T, int32_t H, int32_t max_seq_len, int32_t max_q_len,
+    int32_t D, int32_t interleave, float scale,
+    void* O_part, dcp_dtype_t o_dtype, float* lse_part,
+    void* workspace, size_t workspace_bytes,
+    int32_t* dev_error, void* stream);
+
+/*
+ * dcp_lse_combine over partials in fp32 or bf16 (part_dtype), e.g. those of
+ * dcp_mla_decode_partial_v2 with o_dtype = DCP_DTYPE_BF16.  Everything else
+ * as for dcp_lse_combine; an unsupported part_dtype returns
+ * DCP_ERR_UNSUPPORTED_DTYPE.
+ */
+dcp_status_t dcp_lse_combine_v2(
+    const void* O_part, dcp_dtype_t part_dtype, const float* lse_part,
+    const int32_t* seq_lens, const int32_t* query_start_loc,
+    int32_t B, int32_t T, int32_t H, int32_t D,
+    void* out, dcp_dtype_t out_dtype, float* out_lse, void* stream);
 
 /*
  * The decode step before attention, fused into one launch ["[Kimi-K3] DCP

@@ -37,6 +37,8 @@ def compute_dtype() -> str:
 
 DTYPE_BF16 = 0
 DTYPE_F32 = 1
+KV_BF16 = 0
+KV_FP8_E4M3 = 1
 
 STATUS = {0: "DCP_OK", 1: "DCP_ERR_INVALID_ARG", 2: "DCP_ERR_UNSUPPORTED_DTYPE",
           3: "DCP_ERR_MISALIGNED", 4: "DCP_ERR_TABLE_TOO_NARROW",
@@ -58,6 +60,11 @@ EXPORTS = [
     ("dcp_mla_decode_partial_local", ctypes.c_int,
      [_P, _I64, _P, _I32, _I32, _P, _I32, _I64, _I64, _P, _P, _I32, _I32, _I32, _I32, _I32, _I32, _I32, _I32,
       _I32, _F, _P, _P, _P, _SZ, _P, _P]),
+    ("dcp_mla_decode_partial_v2", ctypes.c_int,
+     [_P, _I64, _P, ctypes.c_int, _P, _I32, _I32, _P, _I32, _I64, _I32, _I64, _I32, _I32, _P, _P, _I32, _I32, _I32,
+      _I32, _I32, _I32, _I32, _F, _P, ctypes.c_int, _P, _P, _SZ, _P, _P]),
+    ("dcp_lse_combine_v2", ctypes.c_int, [_P, ctypes.c_int, _P, _P, _P, _I32, _I32, _I32, _I32, _P, ctypes.c_int, _P,
+                                          _P]),
     ("dcp_decode_concat_cache", ctypes.c_int,
      [_P, _I64, _I64, _P, _I64, _I64, _P, _I64, _P, _I64, _P, _I32, _I32, _P, _I64, _P, _I64, _P, _P]),
     ("dcp_mla_decode_partial_noalloc", ctypes.c_int,
@@ -172,9 +179,11 @@ def _decode_geometry(q, kv_cache, block_table, seq_lens, query_start_loc, O_part
     because the C ABI receives bare pointers: a short block table or a
     flattened cache would otherwise be read past its end on the device.
     Shapes are checked before devices, so the checks run on any host."""
-    args = (("q", q, torch.bfloat16, False), ("kv_cache", kv_cache, torch.bfloat16, True),
+    kv_dt = torch.uint8 if isinstance(kv_cache, torch.Tensor) and kv_cache.dtype == torch.uint8 else torch.bfloat16
+    o_dt = torch.bfloat16 if isinstance(O_part, torch.Tensor) and O_part.dtype == torch.bfloat16 else torch.float32
+    args = (("q", q, torch.bfloat16, False), ("kv_cache", kv_cache, kv_dt, True),
             ("block_table", block_table, torch.int32, False), ("seq_lens", seq_lens, torch.int32, True),
-            ("query_start_loc", query_start_loc, torch.int32, True), ("O_part", O_part, torch.float32, True),
+            ("query_start_loc", query_start_loc, torch.int32, True), ("O_part", O_part, o_dt, True),
             ("lse_part", lse_part, torch.float32, True))
     for name, t, dtype, _ in args:
         if not isinstance(t, torch.Tensor):
@@ -288,6 +297,40 @@ def dcp_mla_decode_partial_local(q, kv_cache, block_table, seq_lens, query_start
     _check(st, "dcp_mla_decode_partial_local")
 
 
+def dcp_mla_decode_partial_v2(q, kv_cache, block_table, seq_lens, query_start_loc, O_part, lse_part, *,
+                              D: int, interleave: int, scale: float, max_seq_len: int, max_q_len: int,
+                              kv_scale: Optional[torch.Tensor] = None, shard_begin: int = 0,
+                              shard_count: Optional[int] = None, workspace: Optional[torch.Tensor] = None,
+                              dev_error: Optional[torch.Tensor] = None, stream=None) -> None:
+    """The general decode: kv_cache bf16, or uint8 FP8 E4M3 codes with
+    kv_scale fp32 [num_blocks, block_size]; block_table [B, W] or per-shard
+    [shard_count, B, W]; O_part fp32 or bf16 [shard_count, T, H, 512]."""
+    if shard_count is None:
+        shard_count = D - shard_begin
+    local = isinstance(block_table, torch.Tensor) and block_table.dim() == 3
+    B, T, H = _decode_geometry(q, kv_cache, block_table, seq_lens, query_start_loc, O_part, lse_part,
+                               shard_count, local=local)
+    fp8 = kv_cache.dtype == torch.uint8
+    if fp8:
+        _need(kv_scale, "kv_scale", torch.float32)
+        if tuple(kv_scale.shape) != tuple(kv_cache.shape[:2]):
+            raise ValueError("kv_scale must be [num_blocks, block_size]")
+    _need_opt(workspace, "workspace", allow_empty=True)
+    if workspace is not None and workspace.numel() == 0:
+        workspace = None
+    _need_opt(dev_error, "dev_error", torch.int32)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    with _Range("dcp_mla_decode_partial_v2"):
+        st = lib().dcp_mla_decode_partial_v2(
+            _ptr(q), q.stride(0), _ptr(kv_cache), KV_FP8_E4M3 if fp8 else KV_BF16, _ptr(kv_scale if fp8 else None),
+            kv_cache.shape[0], kv_cache.shape[1], _ptr(block_table), block_table.shape[-1],
+            block_table.stride(-2), 1 if local else 0, block_table.stride(0) if local else 0, shard_begin,
+            shard_count, _ptr(seq_lens), _ptr(query_start_loc), B, T, H, max_seq_len, max_q_len, D, interleave,
+            scale, _ptr(O_part), DTYPE_BF16 if O_part.dtype == torch.bfloat16 else DTYPE_F32, _ptr(lse_part),
+            _ptr(workspace), ws_bytes, _ptr(dev_error), _stream(stream))
+    _check(st, "dcp_mla_decode_partial_v2")
+
+
 def dcp_mla_decode_partial_noalloc(q, kv_cache, block_table, seq_lens, query_start_loc, O_part, lse_part, *,
                                    D: int, interleave: int, scale: float, max_seq_len: int, max_q_len: int,
                                    dev_error: Optional[torch.Tensor] = None, stream=None) -> None:
@@ -312,7 +355,8 @@ def dcp_lse_combine(O_part, lse_part, seq_lens, query_start_loc, out, out_lse, *
     (bf16 or fp32, by out.dtype) and out_lse fp32 [T, H].  Shapes are checked
     (on any host) before devices: the kernel reads D*T*H*512 floats of O_part
     and indexes query_start_loc up to B."""
-    args = (("O_part", O_part, torch.float32), ("lse_part", lse_part, torch.float32),
+    part_dt = torch.bfloat16 if isinstance(O_part, torch.Tensor) and O_part.dtype == torch.bfloat16 else torch.float32
+    args = (("O_part", O_part, part_dt), ("lse_part", lse_part, torch.float32),
             ("seq_lens", seq_lens, torch.int32), ("query_start_loc", query_start_loc, torch.int32),
             ("out_lse", out_lse, torch.float32))
     for name, t, dtype in args:
@@ -345,10 +389,17 @@ def dcp_lse_combine(O_part, lse_part, seq_lens, query_start_loc, out, out_lse, *
     _need(out, "out", out.dtype)
     if not (out_lse.is_contiguous() or out_lse.data_ptr() == lse_part.data_ptr()):
         raise ValueError("out_lse must be contiguous")
-    with _Range("dcp_lse_combine"):
-        st = lib().dcp_lse_combine(_ptr(O_part), _ptr(lse_part), _ptr(seq_lens), _ptr(query_start_loc), B, T,
-                                   H, D, _ptr(out), dt, _ptr(out_lse), _stream(stream))
-    _check(st, "dcp_lse_combine")
+    if part_dt == torch.float32:
+        with _Range("dcp_lse_combine"):
+            st = lib().dcp_lse_combine(_ptr(O_part), _ptr(lse_part), _ptr(seq_lens), _ptr(query_start_loc), B, T,
+                                       H, D, _ptr(out), dt, _ptr(out_lse), _stream(stream))
+        _check(st, "dcp_lse_combine")
+    else:
+        with _Range("dcp_lse_combine_v2"):
+            st = lib().dcp_lse_combine_v2(_ptr(O_part), DTYPE_BF16, _ptr(lse_part), _ptr(seq_lens),
+                                          _ptr(query_start_loc), B, T, H, D, _ptr(out), dt, _ptr(out_lse),
+                                          _stream(stream))
+        _check(st, "dcp_lse_combine_v2")
 
 
 def dcp_decode_concat_cache(ql_nope, q_pe, kv_c, k_pe, slot_mapping, q_out, kv_cache, *,
@@ -405,7 +456,8 @@ def decode_workspace(B: int, T: int, H: int, D: int, max_seq_len: int, max_q_len
 
 def decode_partial(q, kv_cache, block_table, seq_lens, query_start_loc, D: int, interleave: int,
                    scale: float, max_seq_len: Optional[int] = None, max_q_len: Optional[int] = None,
-                   dev_error: Optional[torch.Tensor] = None, stream=None):
+                   dev_error: Optional[torch.Tensor] = None, stream=None, kv_scale: Optional[torch.Tensor] = None,
+                   out_dtype=torch.float32):
     """Allocating form: returns (O_part fp32 [D, T, H, 512], lse_part fp32 [D, T, H]).
     A 3-D block_table [D, B, W] selects the per-shard layout
     (dcp_mla_decode_partial_local).
@@ -419,9 +471,14 @@ def decode_partial(q, kv_cache, block_table, seq_lens, query_start_loc, D: int, 
         max_seq_len = block_table.shape[-1] * kv_cache.shape[1] * (D if local else 1)
     if max_q_len is None:
         max_q_len = max(1, T)
-    O = torch.empty((D, T, H, LATENT_DIM), dtype=torch.float32, device=q.device)
+    O = torch.empty((D, T, H, LATENT_DIM), dtype=out_dtype, device=q.device)
     lse = torch.empty((D, T, H), dtype=torch.float32, device=q.device)
     ws = decode_workspace(B, T, H, D, max_seq_len, max_q_len, q.device)
+    if kv_cache.dtype == torch.uint8 or out_dtype != torch.float32:
+        dcp_mla_decode_partial_v2(q, kv_cache, block_table, seq_lens, query_start_loc, O, lse, D=D,
+                                  interleave=interleave, scale=scale, max_seq_len=max_seq_len, max_q_len=max_q_len,
+                                  kv_scale=kv_scale, workspace=ws, dev_error=dev_error, stream=stream)
+        return O, lse
     entry = dcp_mla_decode_partial_local if local else dcp_mla_decode_partial
     entry(q, kv_cache, block_table, seq_lens, query_start_loc, O, lse, D=D, interleave=interleave, scale=scale,
           max_seq_len=max_seq_len, max_q_len=max_q_len, workspace=ws, dev_error=dev_error, stream=stream)

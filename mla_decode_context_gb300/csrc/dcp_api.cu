@@ -91,7 +91,7 @@ struct DecodeLaunch {
 };
 
 DecodeLaunch decode_launch(int32_t T, int32_t H, int32_t D, int32_t interleave, int32_t d0, int32_t Dn,
-                           int32_t max_seq_len, bool have_workspace, size_t workspace_bytes) {
+                           int32_t max_seq_len, bool have_workspace, size_t workspace_bytes, bool kv_fp8 = false) {
   DecodeLaunch L{};
   const int sms = dcp::current_sm_count();
   L.plan = dcp::plan_splits(T, D, interleave, d0, Dn, max_seq_len, sms);
@@ -100,6 +100,7 @@ DecodeLaunch decode_launch(int32_t T, int32_t H, int32_t D, int32_t interleave, 
   dcp::DecodeArgs a{};
   a.H = H;
   a.plan = L.plan;
+  a.kv_fp8 = kv_fp8 ? 1 : 0;
   const char* force = std::getenv("DCP_FORCE_SIMT");  // 1: the CUDA-core reference kernel (A/B checks)
   L.simt = (force && force[0] == '1') || !dcp::decode_tc_supported(a);
   const int64_t units = static_cast<int64_t>(T) * Dn * L.plan.splits;
@@ -153,19 +154,24 @@ size_t dcp_decode_workspace_size(int32_t B, int32_t T, int32_t H, int32_t D, int
 }  // extern "C"
 
 static dcp_status_t decode_partial_impl(const void* q, int64_t q_stride_tok, const void* kv_cache,
+                                        dcp_kv_dtype_t kv_dtype, const float* kv_scale,
                                         int32_t num_blocks, int32_t block_size, const int32_t* block_table,
                                         int32_t bt_width, int64_t bt_stride, bool local, int64_t bt_shard_stride,
                                         int32_t d0, int32_t Dn,
                                         const int32_t* seq_lens, const int32_t* query_start_loc, int32_t B,
                                         int32_t T, int32_t H, int32_t max_seq_len, int32_t max_q_len, int32_t D,
-                                        int32_t interleave, float scale, float* O_part, float* lse_part,
-                                        void* workspace, size_t workspace_bytes, int32_t* dev_error, void* stream) {
+                                        int32_t interleave, float scale, void* O_part, dcp_dtype_t o_dtype,
+                                        float* lse_part, void* workspace, size_t workspace_bytes, int32_t* dev_error,
+                                        void* stream) {
   if (B < 0 || T < 0 || H < 1 || H > 1024 || D < 1 || D > DCP_MAX_SHARDS || interleave < 1 ||
       max_seq_len < 0 || max_q_len < 1 || !std::isfinite(scale))
     return DCP_ERR_INVALID_ARG;
   if (B == 0 || T == 0) return DCP_OK;
   if (!q || !kv_cache || !block_table || !seq_lens || !query_start_loc || !O_part || !lse_part)
     return DCP_ERR_INVALID_ARG;
+  if ((kv_dtype != DCP_KV_BF16 && kv_dtype != DCP_KV_FP8_E4M3) || (o_dtype != DCP_DTYPE_F32 && o_dtype != DCP_DTYPE_BF16))
+    return DCP_ERR_UNSUPPORTED_DTYPE;
+  if (kv_dtype == DCP_KV_FP8_E4M3 && !kv_scale) return DCP_ERR_INVALID_ARG;
   if (num_blocks < 1 || block_size < 1 || bt_width < 1 || bt_stride < bt_width ||
       q_stride_tok < static_cast<int64_t>(H) * DCP_KV_DIM)
     return DCP_ERR_INVALID_ARG;
@@ -180,7 +186,8 @@ static dcp_status_t decode_partial_impl(const void* q, int64_t q_stride_tok, con
   if ((covered + block_size - 1) / block_size > bt_width) return DCP_ERR_TABLE_TOO_NARROW;
 
   const DecodeLaunch launch =
-      decode_launch(T, H, D, interleave, d0, Dn, max_seq_len, workspace != nullptr, workspace_bytes);
+      decode_launch(T, H, D, interleave, d0, Dn, max_seq_len, workspace != nullptr, workspace_bytes,
+                    kv_dtype == DCP_KV_FP8_E4M3);
   const dcp::SplitPlan plan = launch.plan;
   const size_t need = launch.need;
   if (need > 0 && (workspace_bytes < need || !workspace)) return DCP_ERR_WORKSPACE_TOO_SMALL;
@@ -190,7 +197,10 @@ static dcp_status_t decode_partial_impl(const void* q, int64_t q_stride_tok, con
   DecodeArgs a{};
   a.q = static_cast<const __nv_bfloat16*>(q);
   a.q_stride_tok = q_stride_tok;
-  a.kv = static_cast<const __nv_bfloat16*>(kv_cache);
+  a.kv = kv_cache;
+  a.kv_fp8 = kv_dtype == DCP_KV_FP8_E4M3 ? 1 : 0;
+  a.kv_scale = kv_scale;
+  a.o_bf16 = o_dtype == DCP_DTYPE_BF16 ? 1 : 0;
   a.num_blocks = num_blocks;
   a.block_size = block_size;
   a.block_table = block_table;
@@ -209,11 +219,11 @@ static dcp_status_t decode_partial_impl(const void* q, int64_t q_stride_tok, con
   a.dev_error = dev_error;
   const char* stall = std::getenv("DCP_TEST_STALL_WAIT");  // failure-path test hook (see DecodeArgs)
   a.stall_test = stall && stall[0] == '1';
-  float* ws_O = nullptr;
+  void* ws_O = nullptr;
   float* ws_lse = nullptr;
   if (plan.splits > 1) {
     const size_t pairs = static_cast<size_t>(plan.splits) * Dn * T * H;
-    ws_O = static_cast<float*>(workspace);
+    ws_O = workspace;  // split partials in the output's dtype (sized for fp32)
     ws_lse = reinterpret_cast<float*>(static_cast<char*>(workspace) +
                                       (pairs * DCP_LATENT_DIM * sizeof(float) + 255) / 256 * 256);
     a.O_dst = ws_O;
@@ -239,8 +249,8 @@ static dcp_status_t decode_partial_impl(const void* q, int64_t q_stride_tok, con
   if (e != cudaSuccess) return DCP_ERR_CUDA;
   if (plan.splits > 1) {
     const int64_t pairs = static_cast<int64_t>(Dn) * T * H;
-    e = dcp::launch_lse_merge_f32(ws_O, ws_lse, pairs * DCP_LATENT_DIM, pairs, plan.splits, pairs, H,
-                                  nullptr, nullptr, 0, /*row_mask=*/false, O_part, lse_part, st);
+    e = dcp::launch_lse_merge(ws_O, a.o_bf16 != 0, ws_lse, pairs * DCP_LATENT_DIM, pairs, plan.splits, pairs, H,
+                              nullptr, nullptr, 0, /*row_mask=*/false, O_part, a.o_bf16 != 0, lse_part, st);
     if (e != cudaSuccess) return DCP_ERR_CUDA;
   }
   return DCP_OK;
@@ -256,9 +266,10 @@ dcp_status_t dcp_mla_decode_partial(const void* q, int64_t q_stride_tok, const v
                                     int32_t max_seq_len, int32_t max_q_len, int32_t D, int32_t interleave,
                                     float scale, float* O_part, float* lse_part, void* workspace,
                                     size_t workspace_bytes, int32_t* dev_error, void* stream) {
-  return decode_partial_impl(q, q_stride_tok, kv_cache, num_blocks, block_size, block_table, bt_width, bt_stride,
-                             false, 0, 0, D, seq_lens, query_start_loc, B, T, H, max_seq_len, max_q_len, D,
-                             interleave, scale, O_part, lse_part, workspace, workspace_bytes, dev_error, stream);
+  return decode_partial_impl(q, q_stride_tok, kv_cache, DCP_KV_BF16, nullptr, num_blocks, block_size, block_table,
+                             bt_width, bt_stride, false, 0, 0, D, seq_lens, query_start_loc, B, T, H, max_seq_len,
+                             max_q_len, D, interleave, scale, O_part, DCP_DTYPE_F32, lse_part, workspace,
+                             workspace_bytes, dev_error, stream);
 }
 
 dcp_status_t dcp_mla_decode_partial_local(const void* q, int64_t q_stride_tok, const void* kv_cache,
@@ -269,10 +280,25 @@ dcp_status_t dcp_mla_decode_partial_local(const void* q, int64_t q_stride_tok, c
                                           int32_t interleave, int32_t shard_begin, int32_t shard_count,
                                           float scale, float* O_part, float* lse_part, void* workspace,
                                           size_t workspace_bytes, int32_t* dev_error, void* stream) {
-  return decode_partial_impl(q, q_stride_tok, kv_cache, num_blocks, block_size, block_table, bt_width, bt_stride,
-                             true, bt_shard_stride, shard_begin, shard_count, seq_lens, query_start_loc, B, T, H,
-                             max_seq_len, max_q_len, D, interleave, scale, O_part, lse_part, workspace,
-                             workspace_bytes, dev_error, stream);
+  return decode_partial_impl(q, q_stride_tok, kv_cache, DCP_KV_BF16, nullptr, num_blocks, block_size, block_table,
+                             bt_width, bt_stride, true, bt_shard_stride, shard_begin, shard_count, seq_lens,
+                             query_start_loc, B, T, H, max_seq_len, max_q_len, D, interleave, scale, O_part,
+                             DCP_DTYPE_F32, lse_part, workspace, workspace_bytes, dev_error, stream);
+}
+
+dcp_status_t dcp_mla_decode_partial_v2(const void* q, int64_t q_stride_tok, const void* kv_cache,
+                                       dcp_kv_dtype_t kv_dtype, const float* kv_scale, int32_t num_blocks,
+                                       int32_t block_size, const int32_t* block_table, int32_t bt_width,
+                                       int64_t bt_stride, int32_t per_shard_tables, int64_t bt_shard_stride,
+                                       int32_t shard_begin, int32_t shard_count, const int32_t* seq_lens,
+                                       const int32_t* query_start_loc, int32_t B, int32_t T, int32_t H,
+                                       int32_t max_seq_len, int32_t max_q_len, int32_t D, int32_t interleave,
+                                       float scale, void* O_part, dcp_dtype_t o_dtype, float* lse_part,
+                                       void* workspace, size_t workspace_bytes, int32_t* dev_error, void* stream) {
+  return decode_partial_impl(q, q_stride_tok, kv_cache, kv_dtype, kv_scale, num_blocks, block_size, block_table,
+                             bt_width, bt_stride, per_shard_tables != 0, bt_shard_stride, shard_begin, shard_count,
+                             seq_lens, query_start_loc, B, T, H, max_seq_len, max_q_len, D, interleave, scale, O_part,
+                             o_dtype, lse_part, workspace, workspace_bytes, dev_error, stream);
 }
 
 int32_t dcp_decode_kernel_launches(int32_t B, int32_t T, int32_t H, int32_t D, int32_t interleave,
@@ -286,11 +312,14 @@ int32_t dcp_decode_kernel_launches(int32_t B, int32_t T, int32_t H, int32_t D, i
   return 1 + (L.plan.splits > 1 ? 1 : 0) + (L.use_order ? 1 : 0);
 }
 
-dcp_status_t dcp_lse_combine(const float* O_part, const float* lse_part, const int32_t* seq_lens,
-                             const int32_t* query_start_loc, int32_t B, int32_t T, int32_t H, int32_t D,
-                             void* out, dcp_dtype_t out_dtype, float* out_lse, void* stream) {
+static dcp_status_t combine_impl(const void* O_part, dcp_dtype_t part_dtype, const float* lse_part,
+                                 const int32_t* seq_lens, const int32_t* query_start_loc, int32_t B, int32_t T,
+                                 int32_t H, int32_t D, void* out, dcp_dtype_t out_dtype, float* out_lse,
+                                 void* stream) {
   if (B < 0 || T < 0 || H < 1 || D < 1 || D > DCP_MAX_SHARDS) return DCP_ERR_INVALID_ARG;
-  if (out_dtype != DCP_DTYPE_BF16 && out_dtype != DCP_DTYPE_F32) return DCP_ERR_UNSUPPORTED_DTYPE;
+  if ((out_dtype != DCP_DTYPE_BF16 && out_dtype != DCP_DTYPE_F32) ||
+      (part_dtype != DCP_DTYPE_BF16 && part_dtype != DCP_DTYPE_F32))
+    return DCP_ERR_UNSUPPORTED_DTYPE;
   if (B == 0 || T == 0) return DCP_OK;
   if (!O_part || !lse_part || !seq_lens || !query_start_loc || !out || !out_lse)
     return DCP_ERR_INVALID_ARG;
@@ -299,18 +328,28 @@ dcp_status_t dcp_lse_combine(const float* O_part, const float* lse_part, const i
   // out must not overlap O_part
   const char* ob = static_cast<const char*>(out);
   const char* oe = ob + pairs * DCP_LATENT_DIM * (out_dtype == DCP_DTYPE_BF16 ? 2 : 4);
-  const char* pb = reinterpret_cast<const char*>(O_part);
-  const char* pe = pb + static_cast<int64_t>(D) * pairs * DCP_LATENT_DIM * 4;
+  const char* pb = static_cast<const char*>(O_part);
+  const char* pe = pb + static_cast<int64_t>(D) * pairs * DCP_LATENT_DIM * (part_dtype == DCP_DTYPE_BF16 ? 2 : 4);
   if (ob < pe && pb < oe) return DCP_ERR_INVALID_ARG;
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
-  cudaError_t e;
-  if (out_dtype == DCP_DTYPE_BF16)
-    e = dcp::launch_lse_merge_bf16(O_part, lse_part, pairs * DCP_LATENT_DIM, pairs, D, pairs, H, seq_lens,
-                                   query_start_loc, B, static_cast<__nv_bfloat16*>(out), out_lse, st);
-  else
-    e = dcp::launch_lse_merge_f32(O_part, lse_part, pairs * DCP_LATENT_DIM, pairs, D, pairs, H, seq_lens,
-                                  query_start_loc, B, true, static_cast<float*>(out), out_lse, st);
+  const cudaError_t e = dcp::launch_lse_merge(O_part, part_dtype == DCP_DTYPE_BF16, lse_part, pairs * DCP_LATENT_DIM,
+                                              pairs, D, pairs, H, seq_lens, query_start_loc, B, /*row_mask=*/true,
+                                              out, out_dtype == DCP_DTYPE_BF16, out_lse, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? DCP_OK : DCP_ERR_CUDA;
+}
+
+dcp_status_t dcp_lse_combine(const float* O_part, const float* lse_part, const int32_t* seq_lens,
+                             const int32_t* query_start_loc, int32_t B, int32_t T, int32_t H, int32_t D,
+                             void* out, dcp_dtype_t out_dtype, float* out_lse, void* stream) {
+  return combine_impl(O_part, DCP_DTYPE_F32, lse_part, seq_lens, query_start_loc, B, T, H, D, out, out_dtype, out_lse,
+                      stream);
+}
+
+dcp_status_t dcp_lse_combine_v2(const void* O_part, dcp_dtype_t part_dtype, const float* lse_part,
+                                const int32_t* seq_lens, const int32_t* query_start_loc, int32_t B, int32_t T,
+                                int32_t H, int32_t D, void* out, dcp_dtype_t out_dtype, float* out_lse,
+                                void* stream) {
+  return combine_impl(O_part, part_dtype, lse_part, seq_lens, query_start_loc, B, T, H, D, out, out_dtype, out_lse,
+                      stream);
 }
 
 dcp_status_t dcp_decode_concat_cache(const void* ql_nope, int64_t ql_nope_stride_tok, int64_t ql_nope_stride_head,

@@ -52,6 +52,16 @@ __device__ __forceinline__ void store4(__nv_bfloat16* p, float4 v) {
   *reinterpret_cast<uint2*>(p) = u;
 }
 
+// 16-byte (fp32) or 8-byte (bf16) streaming load of four partial-output
+// columns, widened to fp32
+__device__ __forceinline__ float4 load4(const float* p) { return __ldcs(reinterpret_cast<const float4*>(p)); }
+__device__ __forceinline__ float4 load4(const __nv_bfloat16* p) {
+  const uint2 u = __ldcs(reinterpret_cast<const uint2*>(p));
+  const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.x));
+  const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.y));
+  return make_float4(a.x, a.y, b.x, b.y);
+}
+
 __device__ __forceinline__ void fma4(float4& acc, float w, const float4& v) {
   acc.x = fmaf(w, v.x, acc.x);
   acc.y = fmaf(w, v.y, acc.y);
@@ -59,9 +69,9 @@ __device__ __forceinline__ void fma4(float4& acc, float w, const float4& v) {
   acc.w = fmaf(w, v.w, acc.w);
 }
 
-template <typename OutT, bool kRowMask, int kBatch>
+template <typename InT, typename OutT, bool kRowMask, int kBatch>
 __global__ void __launch_bounds__(kThreads)
-lse_merge_kernel(const float* __restrict__ O_src, const float* __restrict__ lse_src,
+lse_merge_kernel(const InT* __restrict__ O_src, const float* __restrict__ lse_src,
                  int64_t o_stride, int64_t lse_stride, int nsrc, int64_t npairs, int32_t H,
                  const int32_t* __restrict__ seq_lens, const int32_t* __restrict__ qsl, int32_t B,
                  OutT* __restrict__ out, float* out_lse) {
@@ -75,14 +85,14 @@ lse_merge_kernel(const float* __restrict__ O_src, const float* __restrict__ lse_
   const int64_t pair = static_cast<int64_t>(blockIdx.x) * kPairs + w / kQ;
   const int share = w % kQ;
   const bool has = pair < npairs;
-  const float* src = O_src + pair * kLatent + share * (kLatent / kQ) + 4 * lane;
+  const InT* src = O_src + pair * kLatent + share * (kLatent / kQ) + 4 * lane;
 
   float4 pre[kEarly ? kAllAtOnce : 1];
   const bool early = kEarly && nsrc <= kAllAtOnce;
   if (early && has) {
 #pragma unroll
     for (int k = 0; k < kAllAtOnce; ++k)
-      if (k < nsrc) pre[k] = __ldcs(reinterpret_cast<const float4*>(src + k * o_stride));
+      if (k < nsrc) pre[k] = load4(src + k * o_stride);
   }
 
   // the LSE loads go out together with the row's padding test (a padding
@@ -128,7 +138,7 @@ lse_merge_kernel(const float* __restrict__ O_src, const float* __restrict__ lse_
       for (int i = 0; i < kBatch; ++i)
         if (i < n) {
 #pragma unroll
-          for (int f = 0; f < kF; ++f) v[i][f] = __ldcs(reinterpret_cast<const float4*>(src + ds[i] * o_stride + 128 * f));
+          for (int f = 0; f < kF; ++f) v[i][f] = load4(src + ds[i] * o_stride + 128 * f);
         }
 #pragma unroll
       for (int i = 0; i < kBatch; ++i)
@@ -149,10 +159,10 @@ lse_merge_kernel(const float* __restrict__ O_src, const float* __restrict__ lse_
 template <bool kRowMask>
 constexpr int pairs_per_cta() { return kThreads / 32 / (kRowMask ? 1 : 4); }
 
-template <typename OutT, bool kRowMask, int kBatch>
-cudaError_t launch_batch(const float* O_src, const float* lse_src, int64_t o_stride, int64_t lse_stride,
-                         int nsrc, int64_t npairs, int32_t H, const int32_t* seq_lens, const int32_t* qsl,
-                         int32_t B, OutT* out, float* out_lse, cudaStream_t st) {
+template <typename InT, typename OutT, bool kRowMask, int kBatch>
+cudaError_t launch_batch(const InT* O_src, const float* lse_src, int64_t o_stride, int64_t lse_stride, int nsrc,
+                         int64_t npairs, int32_t H, const int32_t* seq_lens, const int32_t* qsl, int32_t B,
+                         OutT* out, float* out_lse, cudaStream_t st) {
   const int64_t ctas = (npairs + pairs_per_cta<kRowMask>() - 1) / pairs_per_cta<kRowMask>();
   if (ctas > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
   cudaLaunchConfig_t cfg = {};
@@ -164,50 +174,60 @@ cudaError_t launch_batch(const float* O_src, const float* lse_src, int64_t o_str
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, lse_merge_kernel<OutT, kRowMask, kBatch>, O_src, lse_src, o_stride, lse_stride,
-                            nsrc, npairs, H, seq_lens, qsl, B, out, out_lse);
+  return cudaLaunchKernelEx(&cfg, lse_merge_kernel<InT, OutT, kRowMask, kBatch>, O_src, lse_src, o_stride,
+                            lse_stride, nsrc, npairs, H, seq_lens, qsl, B, out, out_lse);
 }
 
 // The combine (one warp per pair, four float4 columns per lane per source)
 // loads two live sources at a time when there are at most two, else four:
 // fewer registers for small D leave room for more pairs per SM.  The split
 // merge (one float4 per lane per source) loads up to 16 at a time.
-template <typename OutT, bool kRowMask>
-cudaError_t launch(const float* O_src, const float* lse_src, int64_t o_stride, int64_t lse_stride,
-                   int nsrc, int64_t npairs, int32_t H, const int32_t* seq_lens, const int32_t* qsl,
-                   int32_t B, OutT* out, float* out_lse, cudaStream_t st) {
+template <typename InT, typename OutT, bool kRowMask>
+cudaError_t launch(const InT* O_src, const float* lse_src, int64_t o_stride, int64_t lse_stride, int nsrc,
+                   int64_t npairs, int32_t H, const int32_t* seq_lens, const int32_t* qsl, int32_t B, OutT* out,
+                   float* out_lse, cudaStream_t st) {
   if (npairs <= 0) return cudaSuccess;
   if constexpr (!kRowMask) {
-    return launch_batch<OutT, kRowMask, 16>(O_src, lse_src, o_stride, lse_stride, nsrc, npairs, H, seq_lens, qsl, B,
-                                            out, out_lse, st);
+    return launch_batch<InT, OutT, kRowMask, 16>(O_src, lse_src, o_stride, lse_stride, nsrc, npairs, H, seq_lens,
+                                                 qsl, B, out, out_lse, st);
   } else {
     if (nsrc <= 2)
-      return launch_batch<OutT, kRowMask, 2>(O_src, lse_src, o_stride, lse_stride, nsrc, npairs, H, seq_lens, qsl, B,
-                                             out, out_lse, st);
-    return launch_batch<OutT, kRowMask, 4>(O_src, lse_src, o_stride, lse_stride, nsrc, npairs, H, seq_lens, qsl, B,
-                                           out, out_lse, st);
+      return launch_batch<InT, OutT, kRowMask, 2>(O_src, lse_src, o_stride, lse_stride, nsrc, npairs, H, seq_lens,
+                                                  qsl, B, out, out_lse, st);
+    return launch_batch<InT, OutT, kRowMask, 4>(O_src, lse_src, o_stride, lse_stride, nsrc, npairs, H, seq_lens,
+                                                qsl, B, out, out_lse, st);
   }
+}
+
+template <typename InT>
+cudaError_t launch_in(const InT* O_src, const float* lse_src, int64_t o_stride, int64_t lse_stride, int nsrc,
+                      int64_t npairs, int32_t H, const int32_t* seq_lens, const int32_t* qsl, int32_t B,
+                      bool row_mask, void* out, bool out_bf16, float* out_lse, cudaStream_t st) {
+  if (row_mask) {
+    if (out_bf16)
+      return launch<InT, __nv_bfloat16, true>(O_src, lse_src, o_stride, lse_stride, nsrc, npairs, H, seq_lens, qsl,
+                                              B, static_cast<__nv_bfloat16*>(out), out_lse, st);
+    return launch<InT, float, true>(O_src, lse_src, o_stride, lse_stride, nsrc, npairs, H, seq_lens, qsl, B,
+                                    static_cast<float*>(out), out_lse, st);
+  }
+  if (out_bf16)
+    return launch<InT, __nv_bfloat16, false>(O_src, lse_src, o_stride, lse_stride, nsrc, npairs, H, seq_lens, qsl,
+                                             B, static_cast<__nv_bfloat16*>(out), out_lse, st);
+  return launch<InT, float, false>(O_src, lse_src, o_stride, lse_stride, nsrc, npairs, H, seq_lens, qsl, B,
+                                   static_cast<float*>(out), out_lse, st);
 }
 
 }  // namespace
 
-cudaError_t launch_lse_merge_bf16(const float* O_src, const float* lse_src, int64_t o_stride,
-                                  int64_t lse_stride, int nsrc, int64_t npairs, int32_t H,
-                                  const int32_t* seq_lens, const int32_t* qsl, int32_t B,
-                                  __nv_bfloat16* out, float* out_lse, cudaStream_t st) {
-  return launch<__nv_bfloat16, true>(O_src, lse_src, o_stride, lse_stride, nsrc, npairs, H,
-                                     seq_lens, qsl, B, out, out_lse, st);
-}
-
-cudaError_t launch_lse_merge_f32(const float* O_src, const float* lse_src, int64_t o_stride,
-                                 int64_t lse_stride, int nsrc, int64_t npairs, int32_t H,
-                                 const int32_t* seq_lens, const int32_t* qsl, int32_t B,
-                                 bool row_mask, float* out, float* out_lse, cudaStream_t st) {
-  if (row_mask)
-    return launch<float, true>(O_src, lse_src, o_stride, lse_stride, nsrc, npairs, H, seq_lens,
-                               qsl, B, out, out_lse, st);
-  return launch<float, false>(O_src, lse_src, o_stride, lse_stride, nsrc, npairs, H, seq_lens,
-                              qsl, B, out, out_lse, st);
+cudaError_t launch_lse_merge(const void* O_src, bool src_bf16, const float* lse_src, int64_t o_stride,
+                             int64_t lse_stride, int nsrc, int64_t npairs, int32_t H, const int32_t* seq_lens,
+                             const int32_t* qsl, int32_t B, bool row_mask, void* out, bool out_bf16,
+                             float* out_lse, cudaStream_t st) {
+  if (src_bf16)
+    return launch_in(static_cast<const __nv_bfloat16*>(O_src), lse_src, o_stride, lse_stride, nsrc, npairs, H,
+                     seq_lens, qsl, B, row_mask, out, out_bf16, out_lse, st);
+  return launch_in(static_cast<const float*>(O_src), lse_src, o_stride, lse_stride, nsrc, npairs, H, seq_lens, qsl,
+                   B, row_mask, out, out_bf16, out_lse, st);
 }
 
 }  // namespace dcp

@@ -276,8 +276,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(DecodeArgs a) {
         if (score) {
           a.lse_dst[pair0 + h] = -INFINITY;
         } else {
-          float4* o = reinterpret_cast<float4*>(a.O_dst + (pair0 + h) * kLatent);
-          for (int i = 0; i < kLatent / 4; ++i) o[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+          // a zero output row: 2 KB in fp32, 1 KB in bf16
+          const int64_t row_bytes = a.o_bf16 ? 2 * kLatent : 4 * kLatent;
+          uint4* o = reinterpret_cast<uint4*>(static_cast<unsigned char*>(a.O_dst) + (pair0 + h) * row_bytes);
+          for (int i = 0; i < row_bytes / 16; ++i) o[i] = make_uint4(0u, 0u, 0u, 0u);
         }
       }
     }
@@ -903,7 +905,6 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(DecodeArgs a) {
       // 32 rows x 32 fp32 per block, rows 144 B apart (16-byte aligned; a
       // warp's 16-byte writes and reads then hit 4 banks groups at most)
       float* scr = reinterpret_cast<float*>(smem + kOffStages) + warp * (32 * 36);
-      float* orow0 = a.O_dst + (pair0 + q4 * 32) * kLatent;
       const int nrows = min(32, a.H - q4 * 32);
       for (int c = c0; c < c0 + 8; ++c) {
         uint32_t o[32];
@@ -915,13 +916,33 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(DecodeArgs a) {
               make_float4(__uint_as_float(o[4 * k]) * inv, __uint_as_float(o[4 * k + 1]) * inv,
                           __uint_as_float(o[4 * k + 2]) * inv, __uint_as_float(o[4 * k + 3]) * inv);
         __syncwarp();
-        // lane l: row 4 m + l / 8, columns 4 (l % 8) .. + 3 of the block
+        if (!a.o_bf16) {
+          // lane l: row 4 m + l / 8, columns 4 (l % 8) .. + 3 of the block
+          float* orow0 = static_cast<float*>(a.O_dst) + (pair0 + q4 * 32) * kLatent;
 #pragma unroll
-        for (int m = 0; m < 8; ++m) {
-          const int rr = 4 * m + (lane >> 3);
-          if (rr < nrows)
-            *reinterpret_cast<float4*>(orow0 + rr * kLatent + 32 * c + 4 * (lane & 7)) =
-                *reinterpret_cast<const float4*>(scr + rr * 36 + 4 * (lane & 7));
+          for (int m = 0; m < 8; ++m) {
+            const int rr = 4 * m + (lane >> 3);
+            if (rr < nrows)
+              *reinterpret_cast<float4*>(orow0 + rr * kLatent + 32 * c + 4 * (lane & 7)) =
+                  *reinterpret_cast<const float4*>(scr + rr * 36 + 4 * (lane & 7));
+          }
+        } else {
+          // bf16 (round to nearest even), lane l: row 8 m + l / 4, columns
+          // 8 (l % 4) .. + 7 of the block: 64 contiguous bytes per row
+          __nv_bfloat16* orow0 = static_cast<__nv_bfloat16*>(a.O_dst) + (pair0 + q4 * 32) * kLatent;
+#pragma unroll
+          for (int m = 0; m < 4; ++m) {
+            const int rr = 8 * m + (lane >> 2);
+            if (rr < nrows) {
+              const float4 x0 = *reinterpret_cast<const float4*>(scr + rr * 36 + 8 * (lane & 3));
+              const float4 x1 = *reinterpret_cast<const float4*>(scr + rr * 36 + 8 * (lane & 3) + 4);
+              __nv_bfloat162 b0 = __floats2bfloat162_rn(x0.x, x0.y), b1 = __floats2bfloat162_rn(x0.z, x0.w);
+              __nv_bfloat162 b2 = __floats2bfloat162_rn(x1.x, x1.y), b3 = __floats2bfloat162_rn(x1.z, x1.w);
+              *reinterpret_cast<uint4*>(orow0 + rr * kLatent + 32 * c + 8 * (lane & 3)) =
+                  make_uint4(*reinterpret_cast<uint32_t*>(&b0), *reinterpret_cast<uint32_t*>(&b1),
+                             *reinterpret_cast<uint32_t*>(&b2), *reinterpret_cast<uint32_t*>(&b3));
+            }
+          }
         }
         __syncwarp();
       }
@@ -1063,7 +1084,7 @@ cudaError_t launch_unit_order(const DecodeArgs& a, int32_t units, int32_t* order
 
 // (Cache rows are addressed in 31 bits: a cache of 2^31 rows would be 2.5 TB.)
 bool decode_tc_supported(const DecodeArgs& a) {
-  return a.H <= 128 && (a.plan.chunk % kTile) == 0 &&
+  return a.H <= 128 && !a.kv_fp8 && (a.plan.chunk % kTile) == 0 &&
          static_cast<int64_t>(a.num_blocks) * a.block_size <= 0x7fffffffLL;
 }
 

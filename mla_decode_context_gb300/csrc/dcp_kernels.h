@@ -13,7 +13,11 @@ namespace dcp {
 struct DecodeArgs {
   const __nv_bfloat16* q;
   int64_t q_stride_tok;  // elements between consecutive rows of q
-  const __nv_bfloat16* kv;
+  // latent cache rows: bf16 [576], or (kv_fp8) FP8 E4M3 codes [576] whose
+  // values are code x kv_scale[row] (one fp32 scale per cache slot)
+  const void* kv;
+  int32_t kv_fp8;
+  const float* kv_scale;
   int32_t num_blocks, block_size;
   const int32_t* block_table;
   int32_t bt_width;
@@ -34,7 +38,8 @@ struct DecodeArgs {
   float scale;
   // Where partials go: O_dst[((s * Dn + d - d0) * T + r) * H + h][512] with s
   // the split (s == 0 only when splits == 1, then O_dst = O_part).
-  float* O_dst;
+  void* O_dst;      // fp32, or bf16 when o_bf16
+  int32_t o_bf16;
   float* lse_dst;
   SplitPlan plan;
   int32_t* dev_error;
@@ -49,16 +54,14 @@ struct DecodeArgs {
 };
 
 // Generic LSE merge over `nsrc` sources: pair p (flattened) reads
-// lse_src[s * lse_stride + p] and O_src[s * o_stride + p * 512 ...].
-// With row masking, pair p belongs to row p / H and padding rows give 0/-inf.
-cudaError_t launch_lse_merge_bf16(const float* O_src, const float* lse_src, int64_t o_stride,
-                                  int64_t lse_stride, int nsrc, int64_t npairs, int32_t H,
-                                  const int32_t* seq_lens, const int32_t* qsl, int32_t B,
-                                  __nv_bfloat16* out, float* out_lse, cudaStream_t st);
-cudaError_t launch_lse_merge_f32(const float* O_src, const float* lse_src, int64_t o_stride,
-                                 int64_t lse_stride, int nsrc, int64_t npairs, int32_t H,
-                                 const int32_t* seq_lens, const int32_t* qsl, int32_t B,
-                                 bool row_mask, float* out, float* out_lse, cudaStream_t st);
+// lse_src[s * lse_stride + p] and O_src[s * o_stride + p * 512 ...] (fp32, or
+// bf16 with src_bf16), and writes out[p * 512 ...] (fp32, or bf16 with
+// out_bf16, round to nearest even) and out_lse[p].  With row masking, pair p
+// belongs to row p / H and padding rows give 0 / -inf.
+cudaError_t launch_lse_merge(const void* O_src, bool src_bf16, const float* lse_src, int64_t o_stride,
+                             int64_t lse_stride, int nsrc, int64_t npairs, int32_t H, const int32_t* seq_lens,
+                             const int32_t* qsl, int32_t B, bool row_mask, void* out, bool out_bf16,
+                             float* out_lse, cudaStream_t st);
 
 // Reference SIMT decode (fp32 FMA, any geometry).
 cudaError_t launch_decode_simt(const DecodeArgs& a, cudaStream_t st);

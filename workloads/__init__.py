@@ -137,13 +137,15 @@ LONG_120K_B2_PREFIX = DecodeSpec("long_ctx_120k_b2_shared_prefix_d8_i1", seed=6,
 LONG_120K_B2_PREFIX_LOCAL = DecodeSpec("long_ctx_120k_b2_shared_prefix_d8_i1_local", seed=6, B=2,
                                        seq_lens=(120_000, 120_000), H=128, block_size=64, D=8, interleave=1,
                                        prefix_len=114_000, shared_prefix=True, layout="local")
+LONG_120K_FP8 = DecodeSpec("long_ctx_120k_b1_d8_i1_fp8", seed=1, B=1, seq_lens=(120_000,), H=128, block_size=64,
+                           D=8, interleave=1, prefix_len=114_000, kv_dtype="fp8_e4m3")
 BATCHED_B64_LOCAL = DecodeSpec("batched_b64_d8_i64_local", seed=2, B=64, seq_lens=("uniform", 1024, 32768), H=128,
                                block_size=64, D=8, interleave=64, layout="local")
 COMBINE_SWEEP = [(D, T) for D in (2, 4, 8) for T in (1, 64, 1024, 4096)]
 COMBINE_H = 128
 
 DECODE_WORKLOADS = {s.name: s for s in (TINY, LONG_120K, BATCHED_B64, SPEC_VERIFY_B32, LONG_120K_B2_PREFIX,
-                                         LONG_120K_B2_PREFIX_LOCAL, BATCHED_B64_LOCAL)}
+                                         LONG_120K_B2_PREFIX_LOCAL, BATCHED_B64_LOCAL, LONG_120K_FP8)}
 
 
 def _threads() -> int:
