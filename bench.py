@@ -43,8 +43,8 @@ KV_ROW_BYTES = 576 * 2
 MEASURED_TRAFFIC = {
     "workload": "long_ctx_120k_b1_d8_i1",
     "source": "mla_decode_context_gb300/csrc/dcp_decode_tc.cu",
-    "sha256": "087b48f9079aa297584983834872647c73c7b55ea0dbce2e4812179de1992fe6",
-    "bytes": 138481152 + 3569664,
+    "sha256": "c02f6fca910868f9a830d8dbb4d8dca211c536349f5fe85e7754d8399be2c6c3",
+    "bytes": 138503168 + 3262976,
 }
 
 
@@ -606,6 +606,22 @@ def run_decode_only(args, spec):
     return 1 if flags else 0
 
 
+def run_combine_only(args):
+    """For profilers: warmup + steps calls of the standalone combine on one
+    combine-sweep point (D, T), nothing timed; exits nonzero on failure."""
+    import torch
+    import mla_decode_context_gb300 as dcp
+    D, T = args.combine_only
+    O, lse, seq, qsl, empty, pad = wl.make_combine_inputs(D, T, device="cuda:0")
+    seq_t, qsl_t = torch.from_numpy(seq).cuda(), torch.from_numpy(qsl).cuda()
+    for _ in range(args.warmup + args.steps):
+        out, out_lse = dcp.lse_combine(O, lse, seq_t, qsl_t)
+    torch.cuda.synchronize()
+    ok = not torch.isnan(out).any().item()
+    print("combine D=%d T=%d: %d calls, finite=%s" % (D, T, args.warmup + args.steps, ok), flush=True)
+    return 0 if ok else 1
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -616,10 +632,14 @@ def main(argv=None):
     ap.add_argument("--decode-only", action="store_true",
                     help="only call the decode warmup + steps times (for ncu captures)")
     ap.add_argument("--eager", action="store_true", help="time eager library calls instead of graph replays")
+    ap.add_argument("--combine-only", type=int, nargs=2, metavar=("D", "T"),
+                    help="only call the standalone combine on one sweep point (for ncu captures)")
     ap.add_argument("--headline-only", action="store_true",
                     help="skip the other workloads and the combine sweep")
     args = ap.parse_args(argv)
     spec = wl.DECODE_WORKLOADS[args.workload]
+    if args.combine_only:
+        return run_combine_only(args)
     if args.decode_only:
         return run_decode_only(args, spec)
     if args.impl == "reference":
