@@ -570,7 +570,7 @@ def run_gb300(args, spec):
                 "config": cfg, "decode_ms_median": dmed, "combine_ms_median": float(np.median(c_ms)),
                 "kv_tokens_per_s": kv_tokens(ob.inp) / ((dmed + float(np.median(c_ms))) * 1e-3),
                 "roofline": ob.roofline(dmed), "gpu_launches_per_step": ob.launches,
-                "kernel": "CUDA cores (fp8 cache)" if other.kv_dtype != "bf16" else "tensor cores"}
+                "kernel": "tensor cores"}
             ob.release()
         recs["combine_sweep_h128"] = combine_sweep_record(dev, flush)
         res["workloads"] = recs

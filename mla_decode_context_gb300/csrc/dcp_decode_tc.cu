@@ -66,6 +66,9 @@
 #include "dcp_kernels.h"
 #include "dcp_sm100.cuh"
 
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
+
 #include <cmath>
 #include <cstring>
 #include <mutex>
@@ -243,6 +246,20 @@ __device__ __forceinline__ void set_abort(Bars& bar, int32_t* dev_error) {
   atomicExch(&bar.abort, 1);
 }
 
+// Two FP8 E4M3 codes -> bf16x2 of code x s.  Exact: E4M3 values convert
+// exactly to half and to fp32, s is a power of two, and a code has at most 4
+// significant bits, so the product (in fp32 range) is exact in bf16 too.
+__device__ __forceinline__ uint32_t e4m3x2_to_bf16x2(uint32_t codes, float s) {
+  const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(codes & 0xffffu), __NV_E4M3);
+  const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&h));
+  __nv_bfloat162 b = __floats2bfloat162_rn(f.x * s, f.y * s);
+  return *reinterpret_cast<uint32_t*>(&b);
+}
+
+// kFp8: the cache holds FP8 E4M3 codes (576 bytes a row) with one fp32 scale
+// per slot; the producers widen them to bf16 on their way into shared
+// memory, so everything downstream is the same as for a bf16 cache.
+template <bool kFp8>
 __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(DecodeArgs a) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   TR_ENTRY();
@@ -421,21 +438,71 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(DecodeArgs a) {
         blk_n[e] = in_n[e] ? __ldg(trow + pos_n[e] / a.block_size) : -1;
       }
     };
-    fetch(group);
-    bool ok = true;
-    if (score) ok = __all_sync(0xffffffffu, mbar_wait(&bar.q_ready, 0));
-    TR_LAP(1, 5);  // producers: waiting for Q to leave the stages
-    for (int j = group; j < ntiles && ok; j += 2) {
-      bool valid[2];
-      int32_t crow[2];
+    // rows of the tile whose block ids are in in_n / pos_n / blk_n
+    auto rows_of = [&](bool (&valid)[2], int32_t (&crow)[2], bool& bad) {
 #pragma unroll
       for (int e = 0; e < 2; ++e) {
         valid[e] = in_n[e] && blk_n[e] >= 0 && blk_n[e] < a.num_blocks;
         // cache row (fits in 31 bits: the library only takes caches of < 2^31 rows)
         crow[e] = valid[e] ? blk_n[e] * a.block_size + pos_n[e] % a.block_size : 0;
       }
-      const bool bad = (in_n[0] && !valid[0]) || (in_n[1] && !valid[1]);
-      if (j + 2 < ntiles) fetch(j + 2);
+      bad = (in_n[0] && !valid[0]) || (in_n[1] && !valid[1]);
+    };
+    // FP8 cache: this thread's codes (8 per row and chunk) and row scales of
+    // a tile, loaded one of the group's tiles ahead of their conversion
+    uint2 codes[2][5];
+    float rscale[2] = {0.f, 0.f};
+    auto load_codes = [&](const bool (&valid)[2], const int32_t (&crow)[2]) {
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const unsigned char* src_row = kvb + static_cast<int64_t>(crow[e]) * kKDim + x * 8;
+        rscale[e] = valid[e] ? __ldg(a.kv_scale + crow[e]) : 0.f;
+#pragma unroll
+        for (int i = 0; i < 5; ++i) {
+          const int c = score ? (i < 4 ? i : 8) : 4 + i;
+          codes[e][i] = (valid[e] && i < nch) ? __ldg(reinterpret_cast<const uint2*>(src_row + c * 64)) : make_uint2(0u, 0u);
+        }
+      }
+    };
+    bool valid_n[2] = {false, false};
+    int32_t crow_n[2] = {0, 0};
+    bool bad_n = false;
+    fetch(group);
+    if constexpr (kFp8) {
+      rows_of(valid_n, crow_n, bad_n);
+      load_codes(valid_n, crow_n);
+      if (group + 2 < ntiles) fetch(group + 2);
+    }
+    bool ok = true;
+    if (score) ok = __all_sync(0xffffffffu, mbar_wait(&bar.q_ready, 0));
+    TR_LAP(1, 5);  // producers: waiting for Q to leave the stages
+    for (int j = group; j < ntiles && ok; j += 2) {
+      bool valid[2];
+      int32_t crow[2];
+      bool bad;
+      uint2 cur[2][5];
+      float cur_scale[2];
+      if constexpr (kFp8) {
+        // this tile's codes were loaded last time round; load the group's
+        // next tile's now, and fetch the block ids of the one after
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          valid[e] = valid_n[e];
+          crow[e] = crow_n[e];
+          cur_scale[e] = rscale[e];
+#pragma unroll
+          for (int i = 0; i < 5; ++i) cur[e][i] = codes[e][i];
+        }
+        bad = bad_n;
+        if (j + 2 < ntiles) {
+          rows_of(valid_n, crow_n, bad_n);
+          load_codes(valid_n, crow_n);
+          if (j + 4 < ntiles) fetch(j + 4);
+        }
+      } else {
+        rows_of(valid, crow, bad);
+        if (j + 2 < ntiles) fetch(j + 2);
+      }
       const int st = j % nslots;
       // the abort flag is read here and tested after this tile's copies are
       // issued, so that its shared-memory latency overlaps them
@@ -474,10 +541,23 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(DecodeArgs a) {
           const int c = score ? (i < 4 ? i : 8) : 4 + i;
           const uint32_t dst = score ? smem_base + stage_chunk_off(st, c) + swz
                                      : smem_base + kOffOwn + st * kHalfBytes + i * kChunkBytes + swz;
-          cp_async16_zfill(dst, src_row + c * 128, src_bytes);
+          if constexpr (kFp8) {
+            // 8 codes -> 8 bf16 (zeros for rows that were not loaded)
+            const uint2 w = cur[e][i];
+            const float sc = cur_scale[e];
+            const uint4 v = make_uint4(e4m3x2_to_bf16x2(w.x, sc), e4m3x2_to_bf16x2(w.x >> 16, sc),
+                                       e4m3x2_to_bf16x2(w.y, sc), e4m3x2_to_bf16x2(w.y >> 16, sc));
+            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+                         : "memory");
+          } else {
+            cp_async16_zfill(dst, src_row + c * 128, src_bytes);
+          }
         }
       }
-      cp_async_mbar_arrive_noinc(&own_loaded[st]);
+      // (fp8: this thread's stores are done; the consumers fence them into
+      // the async proxy after this arrival, as they do the copies')
+      if constexpr (kFp8) mbar_arrive(&own_loaded[st]);
+      else cp_async_mbar_arrive_noinc(&own_loaded[st]);
       TR_LAP(1, 1);  // producers: issuing the copies
       if (__any_sync(0xffffffffu, ab)) {
         ok = false;
@@ -1056,12 +1136,14 @@ int setup_current_device() {
   if (dev < 0 || dev >= kMaxDevices) return 0;
   std::lock_guard<std::mutex> lock(g_setup_mu);
   if (g_resident[dev] > 0) return g_resident[dev];
-  if (cudaFuncSetAttribute(decode_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) !=
-      cudaSuccess) { cudaGetLastError(); return 0; }
+  if (cudaFuncSetAttribute(decode_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) !=
+          cudaSuccess ||
+      cudaFuncSetAttribute(decode_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) !=
+          cudaSuccess) { cudaGetLastError(); return 0; }
   cudaLaunchAttribute attr[1];
   cudaLaunchConfig_t cfg = launch_config(1, nullptr, attr);
   int clusters = 0;
-  if (cudaOccupancyMaxActiveClusters(&clusters, decode_tc_kernel, &cfg) != cudaSuccess || clusters <= 0) {
+  if (cudaOccupancyMaxActiveClusters(&clusters, decode_tc_kernel<false>, &cfg) != cudaSuccess || clusters <= 0) {
     cudaGetLastError();
     return 0;
   }
@@ -1084,9 +1166,23 @@ cudaError_t launch_unit_order(const DecodeArgs& a, int32_t units, int32_t* order
 
 // (Cache rows are addressed in 31 bits: a cache of 2^31 rows would be 2.5 TB.)
 bool decode_tc_supported(const DecodeArgs& a) {
-  return a.H <= 128 && !a.kv_fp8 && (a.plan.chunk % kTile) == 0 &&
+  return a.H <= 128 && (a.plan.chunk % kTile) == 0 &&
          static_cast<int64_t>(a.num_blocks) * a.block_size <= 0x7fffffffLL;
 }
+
+#ifdef DCP_DEBUG_WAITS
+// Debug builds only: the waits that gave up ([count] then [256][4]: barrier
+// shared address, parity, CTA, thread).
+extern "C" int dcp_wait_log_fetch(void* dst, size_t bytes) {
+  unsigned int n = 0;
+  if (cudaMemcpyFromSymbol(&n, sm100::g_dcp_wait_count, sizeof(n)) != cudaSuccess) return -1;
+  if (bytes < 4) return -1;
+  memcpy(dst, &n, 4);
+  size_t rest = bytes - 4;
+  if (rest > sizeof(sm100::g_dcp_wait_log)) rest = sizeof(sm100::g_dcp_wait_log);
+  return static_cast<int>(cudaMemcpyFromSymbol(static_cast<char*>(dst) + 4, sm100::g_dcp_wait_log, rest));
+}
+#endif
 
 #ifdef DCP_TRACE
 // Traced builds only: copy the counters and the per-CTA timeline of the last
@@ -1108,7 +1204,7 @@ cudaError_t launch_decode_tc(const DecodeArgs& a, cudaStream_t st) {
   if (2 * units > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
   cudaLaunchAttribute attr[1];
   cudaLaunchConfig_t cfg = launch_config(units, st, attr);
-  return cudaLaunchKernelEx(&cfg, decode_tc_kernel, a);
+  return a.kv_fp8 ? cudaLaunchKernelEx(&cfg, decode_tc_kernel<true>, a) : cudaLaunchKernelEx(&cfg, decode_tc_kernel<false>, a);
 }
 
 }  // namespace dcp

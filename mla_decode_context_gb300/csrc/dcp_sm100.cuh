@@ -127,15 +127,36 @@ __device__ __forceinline__ bool mbar_test_cluster(uint64_t* bar, uint32_t parity
 // after `limit` polls (each try_wait may itself suspend for a while).
 constexpr uint32_t kWaitLimit = 1u << 22;
 
+#ifdef DCP_DEBUG_WAITS
+// Debug builds only: every wait that gives up logs its barrier's shared
+// address, the parity, the CTA and the thread.
+__device__ unsigned int g_dcp_wait_log[256][4];
+__device__ unsigned int g_dcp_wait_count;
+__device__ __forceinline__ void log_wait_fail(uint64_t* bar, uint32_t parity) {
+  const unsigned int i = atomicAdd(&g_dcp_wait_count, 1u);
+  if (i < 256) {
+    g_dcp_wait_log[i][0] = smem_u32(bar);
+    g_dcp_wait_log[i][1] = parity;
+    g_dcp_wait_log[i][2] = blockIdx.x;
+    g_dcp_wait_log[i][3] = threadIdx.x;
+  }
+}
+#define DCP_LOG_WAIT_FAIL(bar, parity) log_wait_fail(bar, parity)
+#else
+#define DCP_LOG_WAIT_FAIL(bar, parity) do {} while (0)
+#endif
+
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32_t limit = kWaitLimit) {
   for (uint32_t i = 0; i < limit; ++i)
     if (mbar_test(bar, parity)) return true;
+  DCP_LOG_WAIT_FAIL(bar, parity);
   return false;
 }
 
 __device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity, uint32_t limit = kWaitLimit) {
   for (uint32_t i = 0; i < limit; ++i)
     if (mbar_test_cluster(bar, parity)) return true;
+  DCP_LOG_WAIT_FAIL(bar, parity);
   return false;
 }
 
@@ -262,6 +283,26 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
         "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]),
         "=r"(r[30]), "=r"(r[31])
       : "r"(taddr)
+      : "memory");
+}
+
+// 32 lanes x 16 consecutive 32-bit columns.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, "
+      "%14, %15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr)
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, "
+      "%14, %15, %16};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
+      "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
       : "memory");
 }
 

@@ -1,8 +1,8 @@
 """GPU parity of the fp8 latent cache (FP8 E4M3 codes, one fp32 scale per
-slot) and of bf16 partial outputs, against the oracle: the fp8 decode on the
-CUDA-core kernel in both table layouts, bit-exact token selection through
-position-coded fp8 rows, bf16 partials from both kernels (the 120,000-token
-split path included), and the combine over bf16 partials."""
+slot) and of bf16 partial outputs, against the oracle: the fp8 decode on both
+kernels in both table layouts (the 120,000-token split path included),
+bit-exact token selection through position-coded fp8 rows, bf16 partials
+from both kernels, and the combine over bf16 partials."""
 import numpy as np
 import pytest
 import torch
@@ -25,6 +25,15 @@ FP8 = [
     wl.DecodeSpec("fp8_long_split", seed=144, B=1, seq_lens=(9000,), H=128, block_size=64, D=8, interleave=1,
                   kv_dtype="fp8_e4m3"),
 ]
+
+
+@pytest.fixture(params=["tc", "simt"])
+def kernel(request, monkeypatch):
+    if request.param == "simt":
+        monkeypatch.setenv("DCP_FORCE_SIMT", "1")
+    else:
+        monkeypatch.delenv("DCP_FORCE_SIMT", raising=False)
+    return request.param
 
 
 def _decode(inp, t, out_dtype=torch.float32):
@@ -53,13 +62,13 @@ def _check_partials_bf16(O, lse, O_ref, lse_ref, what):
 
 
 @pytest.mark.parametrize("spec", FP8, ids=lambda s: s.name)
-def test_fp8_decode_matches_oracle(spec):
+def test_fp8_decode_matches_oracle(spec, kernel):
     inp = wl.make_decode_inputs(spec)
     t = G.to_device(inp)
     O, lse, err = _decode(inp, t)
     assert err == 0
     O_ref, lse_ref, rows = oracle.decode_partial(inp)
-    G.check_partials(O.cpu().numpy(), lse.cpu().numpy(), O_ref, lse_ref, spec.name)
+    G.check_partials(O.cpu().numpy(), lse.cpu().numpy(), O_ref, lse_ref, "%s/%s" % (spec.name, kernel))
     out, out_lse = G.run_combine(O, lse, t)
     _, _, pad = oracle.row_lengths(inp["seq_lens"], inp["query_start_loc"], inp["T"])
     out_ref, out_lse_ref = oracle.lse_combine(O_ref, lse_ref, pad)
@@ -67,7 +76,7 @@ def test_fp8_decode_matches_oracle(spec):
 
 
 @pytest.mark.parametrize("spec", [FP8[0], FP8[2]], ids=lambda s: s.name)
-def test_fp8_walker_bit_exact(spec):
+def test_fp8_walker_bit_exact(spec, kernel):
     # position digits are exact in E4M3 with a power-of-two scale
     inp = wl.make_decode_inputs(spec, kv_rows=PC.kv_rows)
     inp["scale"] = 0.0
@@ -75,7 +84,7 @@ def test_fp8_walker_bit_exact(spec):
     O, lse, err = _decode(inp, t)
     assert err == 0
     n, E, _ = PC.expected(inp)
-    PC.check(O.cpu().numpy(), lse.cpu().numpy(), n, E, spec.name)
+    PC.check(O.cpu().numpy(), lse.cpu().numpy(), n, E, "%s/%s" % (spec.name, kernel))
 
 
 BF16_OUT = [
@@ -84,15 +93,6 @@ BF16_OUT = [
     wl.DecodeSpec("bf16out_q4_causal_padding_local", seed=153, B=4, seq_lens=(0, 2, 903, 4), q_len=4, H=128,
                   block_size=64, D=8, interleave=1, extra_rows=2, layout="local"),
 ]
-
-
-@pytest.fixture(params=["tc", "simt"])
-def kernel(request, monkeypatch):
-    if request.param == "simt":
-        monkeypatch.setenv("DCP_FORCE_SIMT", "1")
-    else:
-        monkeypatch.delenv("DCP_FORCE_SIMT", raising=False)
-    return request.param
 
 
 @pytest.mark.parametrize("spec", BF16_OUT, ids=lambda s: s.name)
@@ -107,6 +107,17 @@ def test_bf16_partials_match_oracle(spec, kernel):
     _, _, pad = oracle.row_lengths(inp["seq_lens"], inp["query_start_loc"], inp["T"])
     out_ref, out_lse_ref = oracle.lse_combine(O_ref, lse_ref, pad)
     G.check_combined(out.float().cpu().numpy(), out_lse.cpu().numpy(), out_ref, out_lse_ref, pad, spec.name)
+
+
+def test_fp8_long_context_120k():
+    """The 120,000-token context in the fp8 cache, on the tensor cores (nine
+    splits per shard), against the oracle."""
+    inp = wl.make_decode_inputs(wl.LONG_120K_FP8)
+    t = G.to_device(inp)
+    O, lse, err = _decode(inp, t)
+    assert err == 0
+    O_ref, lse_ref, rows = oracle.decode_partial(inp)
+    G.check_partials(O.cpu().numpy(), lse.cpu().numpy(), O_ref, lse_ref, "120k fp8")
 
 
 def test_bf16_partials_long_context_120k():
