@@ -212,6 +212,9 @@ static dcp_status_t decode_partial_impl(const void* q, int64_t q_stride_tok, con
   a.qsl = query_start_loc;
   a.B = B; a.T = T; a.H = H;
   a.max_seq_len = max_seq_len; a.max_q_len = max_q_len;
+  // a request's verification rows side by side (when the rows split evenly
+  // into groups of max_q_len: a permutation of the units either way)
+  a.row_group = (max_q_len >= 2 && max_q_len <= 8 && T % max_q_len == 0) ? max_q_len : 1;
   a.D = D; a.I = interleave;
   a.d0 = d0; a.Dn = Dn;
   a.scale = scale;

@@ -272,10 +272,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(DecodeArgs a) {
   const uint32_t peer = cta ^ 1u;
 
   const int64_t unit = a.unit_order ? __ldg(a.unit_order + (blockIdx.x >> 1)) : (blockIdx.x >> 1);
-  const int per_row = a.Dn * a.plan.splits;
-  const int r = static_cast<int>(unit / per_row);
-  const int d = a.d0 + static_cast<int>((unit % per_row) / a.plan.splits);  // shard (of D)
-  const int s = static_cast<int>(unit % a.plan.splits);
+  const UnitCoords uc = unit_coords(a, unit);
+  const int r = uc.r;
+  const int d = a.d0 + uc.dd;  // shard (of D)
+  const int s = uc.s;
 
   const RowInfo ri = resolve_row(a.seq_lens, a.qsl, a.B, r, a.max_seq_len, a.max_q_len);
   if (ri.err && threadIdx.x == 0 && cta == 0 && d == a.d0 && s == 0) report(a.dev_error, ri.err);
@@ -1062,8 +1062,8 @@ __global__ void __launch_bounds__(1024) unit_order_kernel(DecodeArgs a, int32_t 
   __shared__ int32_t wcnt[32][33];
   const int t = threadIdx.x, w = t >> 5, lane = t & 31;
   auto key_of = [&](int32_t u) -> int {
-    const int per_row = a.Dn * a.plan.splits;
-    const int r = u / per_row, d = a.d0 + (u % per_row) / a.plan.splits, s = u % a.plan.splits;
+    const UnitCoords uc = unit_coords(a, u);
+    const int r = uc.r, d = a.d0 + uc.dd, s = uc.s;
     const RowInfo ri = resolve_row(a.seq_lens, a.qsl, a.B, r, a.max_seq_len, a.max_q_len);
     const int32_t n = ri.padding ? 0 : local_len(ri.L, d, a.D, a.I);
     const int32_t lo = s * a.plan.chunk, hi = min(n, lo + a.plan.chunk);

@@ -46,12 +46,33 @@ struct DecodeArgs {
   // Optional launch order of the tensor-core decode's units (cluster c runs
   // unit unit_order[c]); nullptr = index order.
   const int32_t* unit_order;
+  // Rows per group of the unit index (1, or the verification width when
+  // every request has that many rows): see unit_coords.
+  int32_t row_group;
   // Test hook for the failure path (0 in normal use): nonzero makes the
   // tensor-core decode's first softmax group wait on a barrier that nothing
   // completes, so every unit ends through its bounded waits and reports
   // DCP_DEVERR_TIMEOUT.
   int32_t stall_test;
 };
+
+// The (row, shard - d0, split) of unit u of the tensor-core decode, with the
+// rows of each group of row_group consecutive rows innermost: u = ((row /
+// row_group x Dn + shard - d0) x splits + split) x row_group + row %
+// row_group.  With row_group = the requests' verification width, a request's
+// rows for one (shard, split) run side by side and read each KV tile from L2
+// at the same time, so the request's KV comes from HBM about once.
+struct UnitCoords {
+  int32_t r, dd, s;
+};
+__device__ __forceinline__ UnitCoords unit_coords(const DecodeArgs& a, int64_t u) {
+  const int64_t g = a.row_group > 1 ? a.row_group : 1;
+  const int64_t i = u % g, rest = u / g;
+  const int32_t s = static_cast<int32_t>(rest % a.plan.splits);
+  const int64_t rest2 = rest / a.plan.splits;
+  const int32_t dd = static_cast<int32_t>(rest2 % a.Dn);
+  return UnitCoords{static_cast<int32_t>((rest2 / a.Dn) * g + i), dd, s};
+}
 
 // Generic LSE merge over `nsrc` sources: pair p (flattened) reads
 // lse_src[s * lse_stride + p] and O_src[s * o_stride + p * 512 ...] (fp32, or
