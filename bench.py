@@ -43,8 +43,8 @@ KV_ROW_BYTES = 576 * 2
 MEASURED_TRAFFIC = {
     "workload": "long_ctx_120k_b1_d8_i1",
     "source": "mla_decode_context_gb300/csrc/dcp_decode_tc.cu",
-    "sha256": "c02f6fca910868f9a830d8dbb4d8dca211c536349f5fe85e7754d8399be2c6c3",
-    "bytes": 138503168 + 3262976,
+    "sha256": "f7262c923063fb1717ec20e77ec97aa07ab3f4bae255fd4f00f4c51094e01cf8",
+    "bytes": 138479104 + 3334912,
 }
 
 
@@ -598,11 +598,13 @@ def run_decode_only(args, spec):
     for _ in range(args.warmup + args.steps):
         dcp.decode_partial(t["q"], t["kv_cache"], t["block_table"], t["seq_lens"], t["query_start_loc"],
                            D=inp["D"], interleave=inp["interleave"], scale=inp["scale"],
-                           max_seq_len=inp["max_seq_len"], max_q_len=inp["max_q_len"], dev_error=err)
+                           max_seq_len=inp["max_seq_len"], max_q_len=inp["max_q_len"], dev_error=err,
+                           kv_scale=t.get("kv_scale"))
     torch.cuda.synchronize()
     flags = int(err.item())
+    row_bytes = 576 + 4 if inp.get("kv_dtype", "bf16") == "fp8_e4m3" else KV_ROW_BYTES
     print("%s: %d decode calls, dev_error 0x%x, KV bytes %d"
-          % (spec.name, args.warmup + args.steps, flags, kv_tokens(inp) * KV_ROW_BYTES), flush=True)
+          % (spec.name, args.warmup + args.steps, flags, kv_tokens(inp) * row_bytes), flush=True)
     return 1 if flags else 0
 
 
