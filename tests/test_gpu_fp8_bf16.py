@@ -109,6 +109,19 @@ def test_bf16_partials_match_oracle(spec, kernel):
     G.check_combined(out.float().cpu().numpy(), out_lse.cpu().numpy(), out_ref, out_lse_ref, pad, spec.name)
 
 
+@pytest.mark.parametrize("spec", [FP8[1], FP8[2]], ids=lambda s: s.name)
+def test_fp8_cache_with_bf16_partials(spec, kernel):
+    """Both options at once: the fp8 cache widened on the way in, bf16
+    partials on the way out (causal verification rows with padding, and the
+    per-shard layout with an unaligned interleave)."""
+    inp = wl.make_decode_inputs(spec)
+    t = G.to_device(inp)
+    O, lse, err = _decode(inp, t, out_dtype=torch.bfloat16)
+    assert err == 0 and O.dtype == torch.bfloat16
+    O_ref, lse_ref, rows = oracle.decode_partial(inp)
+    _check_partials_bf16(O, lse, O_ref, lse_ref, "%s/%s" % (spec.name, kernel))
+
+
 def test_fp8_long_context_120k():
     """The 120,000-token context in the fp8 cache, on the tensor cores (nine
     splits per shard), against the oracle."""
