@@ -5,19 +5,25 @@
 // kQ warps own one (row, head) pair, each a 512 / kQ-column share of its
 // output, 8 / kQ pairs per CTA.  Lane d of each warp reads source d's LSE,
 // the live set E = {d : lse_d != -inf} is a warp ballot, and the weights
-// exp2(lse_d log2 e - M) (M = max over E) are warp reductions; the partial
-// output of a masked source is never loaded ["[Kimi-K3] DCP support" summary
-// on prhub.com.cn, implementation step 4: -inf at the source, zero-weight
+// exp2(lse_d log2 e - M) (M = max over E) are warp reductions; a masked
+// source adds nothing to the sum ["[Kimi-K3] DCP support" summary on
+// prhub.com.cn, implementation step 4: -inf at the source, zero-weight
 // sources skipped by the consumer].  Lane t owns kF = 4 / kQ float4 columns
 // of each source (columns 4t + 128k of its warp's share), so every load and
-// store of a warp is a contiguous 512-byte access.
-//   combine (row mask): kQ = 1, one warp per pair, so many pairs per SM keep
-//     enough bytes in flight; the loads of kBatch live sources go out at once.
-//   split merge: kQ = 4, one float4 per source per lane, and since every
-//     split partial is finite (zeros and LSE -inf when its split held no
-//     token) the loads of up to 16 sources start before the weights are
-//     known: one memory round trip.
-// Sources are summed in increasing index order, so results are
+// store of a warp is a contiguous 512-byte access.  Two ways to load:
+//   batched (kEarly = false): after the weights, the live sources only,
+//     kBatch at a time.  A masked source's partial is never read.  The
+//     combine takes this way with one warp per pair when there are many
+//     pairs, so that many pairs per SM keep enough bytes in flight.
+//   early (kEarly = true): every source's partial is loaded before the
+//     weights are known (one memory round trip in all) and the sum takes the
+//     live ones only, so the bytes of a masked source (NaN or anything) are
+//     read but never used.  The split merge (up to 16 splits) and the
+//     combine of few pairs take this way: two warps per pair up to 8 or 12
+//     sources, four warps up to 16; a thread holds at most 96 loaded
+//     registers and two 256-thread CTAs fit on an SM.
+// Both ways sum the live sources in increasing index order with the same
+// weights, so they give bit-identical results and every result is
 // deterministic.  The kernel waits on the grid it depends on (programmatic
 // dependent launch) only after its launch, so its launch overlaps the tail of
 // the kernel that produced its inputs.
@@ -69,17 +75,16 @@ __device__ __forceinline__ void fma4(float4& acc, float w, const float4& v) {
   acc.w = fmaf(w, v.w, acc.w);
 }
 
-template <typename InT, typename OutT, bool kRowMask, int kBatch>
-__global__ void __launch_bounds__(kThreads)
+// kQ warps per pair; the early way loads all nsrc <= kBatch sources at once,
+// the batched way kBatch live sources at a time
+template <typename InT, typename OutT, bool kRowMask, bool kEarly, int kQ, int kBatch>
+__global__ void __launch_bounds__(kThreads, (!kEarly && kBatch <= 2) ? 4 : 2)
 lse_merge_kernel(const InT* __restrict__ O_src, const float* __restrict__ lse_src,
                  int64_t o_stride, int64_t lse_stride, int nsrc, int64_t npairs, int32_t H,
                  const int32_t* __restrict__ seq_lens, const int32_t* __restrict__ qsl, int32_t B,
                  OutT* __restrict__ out, float* out_lse) {
-  constexpr int kQ = kRowMask ? 1 : 4;          // warps per pair
   constexpr int kF = 4 / kQ;                     // float4 columns per lane per source
   constexpr int kPairs = kThreads / 32 / kQ;     // pairs per CTA
-  constexpr bool kEarly = !kRowMask;
-  constexpr int kAllAtOnce = 16;                 // split merge: sources loaded before the weights
   asm volatile("griddepcontrol.wait;" ::: "memory");  // inputs written by the preceding grid
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
   const int64_t pair = static_cast<int64_t>(blockIdx.x) * kPairs + w / kQ;
@@ -87,12 +92,14 @@ lse_merge_kernel(const InT* __restrict__ O_src, const float* __restrict__ lse_sr
   const bool has = pair < npairs;
   const InT* src = O_src + pair * kLatent + share * (kLatent / kQ) + 4 * lane;
 
-  float4 pre[kEarly ? kAllAtOnce : 1];
-  const bool early = kEarly && nsrc <= kAllAtOnce;
-  if (early && has) {
+  float4 pre[kEarly ? kBatch : 1][kF];
+  if (kEarly && has) {
 #pragma unroll
-    for (int k = 0; k < kAllAtOnce; ++k)
-      if (k < nsrc) pre[k] = load4(src + k * o_stride);
+    for (int k = 0; k < (kEarly ? kBatch : 1); ++k)
+      if (k < nsrc) {
+#pragma unroll
+        for (int f = 0; f < kF; ++f) pre[k][f] = load4(src + k * o_stride + 128 * f);
+      }
   }
 
   // the LSE loads go out together with the row's padding test (a padding
@@ -117,11 +124,15 @@ lse_merge_kernel(const InT* __restrict__ O_src, const float* __restrict__ lse_sr
   float4 acc[kF];
 #pragma unroll
   for (int f = 0; f < kF; ++f) acc[f] = make_float4(0.f, 0.f, 0.f, 0.f);
-  if (early) {
-    // in increasing source index; a masked source adds 0 * finite
+  if (kEarly) {
+    // the live sources in increasing index (a padding row has none)
 #pragma unroll
-    for (int k = 0; k < kAllAtOnce; ++k)
-      if (k < nsrc) fma4(acc[0], __shfl_sync(kFull, wt, k), pre[k]);
+    for (int k = 0; k < (kEarly ? kBatch : 1); ++k)
+      if (k < nsrc && ((live_mask >> k) & 1u)) {
+        const float wd = __shfl_sync(kFull, wt, k);
+#pragma unroll
+        for (int f = 0; f < kF; ++f) fma4(acc[f], wd, pre[k][f]);
+      }
   } else {
     unsigned m = live_mask;  // padding row or no live source: m == 0, so zeros
     while (m) {
@@ -156,14 +167,12 @@ lse_merge_kernel(const InT* __restrict__ O_src, const float* __restrict__ lse_sr
     store4(dst + 128 * f, make_float4(acc[f].x * inv, acc[f].y * inv, acc[f].z * inv, acc[f].w * inv));
 }
 
-template <bool kRowMask>
-constexpr int pairs_per_cta() { return kThreads / 32 / (kRowMask ? 1 : 4); }
-
-template <typename InT, typename OutT, bool kRowMask, int kBatch>
+template <typename InT, typename OutT, bool kRowMask, bool kEarly, int kQ, int kBatch>
 cudaError_t launch_batch(const InT* O_src, const float* lse_src, int64_t o_stride, int64_t lse_stride, int nsrc,
                          int64_t npairs, int32_t H, const int32_t* seq_lens, const int32_t* qsl, int32_t B,
                          OutT* out, float* out_lse, cudaStream_t st) {
-  const int64_t ctas = (npairs + pairs_per_cta<kRowMask>() - 1) / pairs_per_cta<kRowMask>();
+  constexpr int kPairs = kThreads / 32 / kQ;
+  const int64_t ctas = (npairs + kPairs - 1) / kPairs;
   if (ctas > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(ctas));
@@ -174,29 +183,53 @@ cudaError_t launch_batch(const InT* O_src, const float* lse_src, int64_t o_strid
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, lse_merge_kernel<InT, OutT, kRowMask, kBatch>, O_src, lse_src, o_stride,
-                            lse_stride, nsrc, npairs, H, seq_lens, qsl, B, out, out_lse);
+  return cudaLaunchKernelEx(&cfg, lse_merge_kernel<InT, OutT, kRowMask, kEarly, kQ, kBatch>, O_src, lse_src,
+                            o_stride, lse_stride, nsrc, npairs, H, seq_lens, qsl, B, out, out_lse);
 }
 
-// The combine (one warp per pair, four float4 columns per lane per source)
-// loads two live sources at a time when there are at most two, else four:
-// fewer registers for small D leave room for more pairs per SM.  The split
-// merge (one float4 per lane per source) loads up to 16 at a time.
+// Below this many pairs one warp per pair leaves most SMs idle (eight pairs
+// per 256-thread CTA), and the combine loads early instead.
+constexpr int64_t kFewPairs = 2048;
+
+// The early way: all sources at once, two warps per pair up to 12 sources,
+// four up to 16; past 16 the batched way with four warps per pair.
+template <typename InT, typename OutT, bool kRowMask>
+cudaError_t launch_early(const InT* O_src, const float* lse_src, int64_t o_stride, int64_t lse_stride, int nsrc,
+                         int64_t npairs, int32_t H, const int32_t* seq_lens, const int32_t* qsl, int32_t B,
+                         OutT* out, float* out_lse, cudaStream_t st) {
+  if (nsrc <= 8)
+    return launch_batch<InT, OutT, kRowMask, true, 2, 8>(O_src, lse_src, o_stride, lse_stride, nsrc, npairs, H,
+                                                         seq_lens, qsl, B, out, out_lse, st);
+  if (nsrc <= 12)
+    return launch_batch<InT, OutT, kRowMask, true, 2, 12>(O_src, lse_src, o_stride, lse_stride, nsrc, npairs, H,
+                                                          seq_lens, qsl, B, out, out_lse, st);
+  if (nsrc <= 16)
+    return launch_batch<InT, OutT, kRowMask, true, 4, 16>(O_src, lse_src, o_stride, lse_stride, nsrc, npairs, H,
+                                                          seq_lens, qsl, B, out, out_lse, st);
+  return launch_batch<InT, OutT, kRowMask, false, 4, 16>(O_src, lse_src, o_stride, lse_stride, nsrc, npairs, H,
+                                                         seq_lens, qsl, B, out, out_lse, st);
+}
+
+// The split merge loads early.  The combine of many pairs (one warp per pair,
+// four float4 columns per lane per source) loads two live sources at a time
+// when there are at most two, else four: fewer registers for small D leave
+// room for more pairs per SM.
 template <typename InT, typename OutT, bool kRowMask>
 cudaError_t launch(const InT* O_src, const float* lse_src, int64_t o_stride, int64_t lse_stride, int nsrc,
                    int64_t npairs, int32_t H, const int32_t* seq_lens, const int32_t* qsl, int32_t B, OutT* out,
                    float* out_lse, cudaStream_t st) {
   if (npairs <= 0) return cudaSuccess;
-  if constexpr (!kRowMask) {
-    return launch_batch<InT, OutT, kRowMask, 16>(O_src, lse_src, o_stride, lse_stride, nsrc, npairs, H, seq_lens,
-                                                 qsl, B, out, out_lse, st);
-  } else {
+  if (!kRowMask || npairs < kFewPairs)
+    return launch_early<InT, OutT, kRowMask>(O_src, lse_src, o_stride, lse_stride, nsrc, npairs, H, seq_lens, qsl,
+                                             B, out, out_lse, st);
+  if constexpr (kRowMask) {
     if (nsrc <= 2)
-      return launch_batch<InT, OutT, kRowMask, 2>(O_src, lse_src, o_stride, lse_stride, nsrc, npairs, H, seq_lens,
-                                                  qsl, B, out, out_lse, st);
-    return launch_batch<InT, OutT, kRowMask, 4>(O_src, lse_src, o_stride, lse_stride, nsrc, npairs, H, seq_lens,
-                                                qsl, B, out, out_lse, st);
+      return launch_batch<InT, OutT, kRowMask, false, 1, 2>(O_src, lse_src, o_stride, lse_stride, nsrc, npairs, H,
+                                                            seq_lens, qsl, B, out, out_lse, st);
+    return launch_batch<InT, OutT, kRowMask, false, 1, 4>(O_src, lse_src, o_stride, lse_stride, nsrc, npairs, H,
+                                                          seq_lens, qsl, B, out, out_lse, st);
   }
+  return cudaSuccess;
 }
 
 template <typename InT>

@@ -54,6 +54,22 @@ def test_combine_sweep(D, T, out_dtype):
         assert np.all(np.abs(got - ref) <= G.bf16_ulp(ref) + G.COMB_REL * scale)
 
 
+@pytest.mark.parametrize("D", [2, 8, 12, 16, 32])
+def test_combine_few_and_many_pairs_agree_bitwise(D):
+    """Few (row, head) pairs load every source before the weights, many load
+    the live ones in batches after them: the same live sources in the same
+    order with the same weights, so the rows they share are bit-identical
+    (empty shards' NaN payloads and padding rows included)."""
+    T, n = 64, 8  # 8192 pairs, and 1024 in the first 8 rows
+    O, lse, seq, qsl, pad = _inputs(D, T, seed=101)
+    full, full_lse = dcp.lse_combine(O, lse, seq, qsl, out_dtype=torch.float32)
+    few, few_lse = dcp.lse_combine(O[:, :n].contiguous(), lse[:, :n].contiguous(), seq[:n].contiguous(),
+                                   qsl[:n + 1].contiguous(), out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    assert not torch.isnan(full).any()
+    assert torch.equal(full[:n], few) and torch.equal(full_lse[:n], few_lse)
+
+
 def test_combine_shard_order_invariance():
     O, lse, seq, qsl, pad = _inputs(8, 1024)
     a, al = dcp.lse_combine(O, lse, seq, qsl, out_dtype=torch.float32)

@@ -80,6 +80,24 @@ def test_decode_matches_oracle(spec, kernel):
     _full_check(wl.make_decode_inputs(spec))
 
 
+SPLIT_COUNTS = {1500: 6, 2300: 9, 2900: 12, 3900: 16}
+
+
+@pytest.mark.parametrize("n", sorted(SPLIT_COUNTS), ids=lambda n: "%d_splits" % SPLIT_COUNTS[n])
+def test_split_merge_source_counts(n, kernel):
+    """One shard of n tokens splits into 6, 9, 12 or 16 chunks of 256: each
+    count takes another shape of the split merge (two warps per pair up to 8
+    and up to 12 sources, four warps up to 16).  The second request is short,
+    so most of its splits are empty and merge as zero-weight sources."""
+    spec = wl.DecodeSpec("h128_d1_%d" % n, seed=43, B=2, seq_lens=(n, 100), H=128, block_size=64, D=1,
+                         interleave=1)
+    inp = wl.make_decode_inputs(spec)
+    # the decode and the split merge (plus the unit-order kernel when units
+    # outnumber the clusters of one wave)
+    assert dcp.dcp_decode_kernel_launches(inp["B"], inp["T"], 128, 1, 1, inp["max_seq_len"], 1, 1 << 30) >= 2
+    _full_check(inp)
+
+
 def test_decode_is_deterministic(kernel):
     inp = wl.make_decode_inputs(SMALL[1])
     t = G.to_device(inp)
