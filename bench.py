@@ -678,6 +678,15 @@ def run_combine_only(args):
     return 0 if ok else 1
 
 
+def run_probe(name: str) -> int:
+    """The measurements behind the kernels' design choices: each probe is a
+    small CUDA program (bounded waits, one CTA per SM) that prints its own
+    table."""
+    from mla_decode_context_gb300 import build_lib
+    exe = build_lib.build_probe(name)
+    return subprocess.run([exe], check=False).returncode
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -692,7 +701,12 @@ def main(argv=None):
                     help="only call the standalone combine on one sweep point (for ncu captures)")
     ap.add_argument("--headline-only", action="store_true",
                     help="skip the other workloads and the combine sweep")
+    ap.add_argument("--probe", choices=["mma_rate", "load_rate", "tma_rate"],
+                    help="build and run one stand-alone hardware-rate probe (tensor-core issue rate, "
+                         "cp.async streaming rate, TMA streaming rate) instead of the bench")
     args = ap.parse_args(argv)
+    if args.probe:
+        return run_probe(args.probe)
     spec = wl.DECODE_WORKLOADS[args.workload]
     if args.combine_only:
         return run_combine_only(args)

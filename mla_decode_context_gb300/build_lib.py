@@ -82,5 +82,25 @@ def build(verbose: bool = False, force: bool = False, ptxas_info: bool = False) 
     return LIB
 
 
+PROBES = ("mma_rate", "load_rate", "tma_rate")
+
+
+def build_probe(name: str) -> str:
+    """Compile the stand-alone measurement program csrc/probes/<name>.cu (not
+    part of the library) and return the path of the executable."""
+    if name not in PROBES:
+        raise ValueError("unknown probe %r (one of %s)" % (name, ", ".join(PROBES)))
+    src = os.path.join(CSRC, "probes", name + ".cu")
+    out_dir = os.path.join(BUILD, "probes")
+    os.makedirs(out_dir, exist_ok=True)
+    exe = os.path.join(out_dir, name)
+    if _stale(exe, [src]):
+        cmd = [nvcc()] + ARCH + ["-O3", "-std=c++17", "-o", exe, src]
+        p = subprocess.run(cmd, capture_output=True, text=True)
+        if p.returncode != 0:
+            raise RuntimeError("nvcc failed on %s:\n%s\n%s" % (src, " ".join(cmd), p.stderr))
+    return exe
+
+
 if __name__ == "__main__":
     print(build(verbose=True, force="--force" in sys.argv, ptxas_info="--ptxas" in sys.argv))
