@@ -216,6 +216,8 @@ static dcp_status_t decode_partial_impl(const void* q, int64_t q_stride_tok, con
   // into groups of max_q_len: a permutation of the units either way)
   a.row_group = (max_q_len >= 2 && max_q_len <= 8 && T % max_q_len == 0) ? max_q_len : 1;
   a.D = D; a.I = interleave;
+  a.div_I = dcp::make_fastdiv(interleave);
+  a.div_bs = dcp::make_fastdiv(block_size);
   a.d0 = d0; a.Dn = Dn;
   a.scale = scale;
   a.plan = plan;

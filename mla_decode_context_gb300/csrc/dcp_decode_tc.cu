@@ -434,8 +434,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(DecodeArgs a) {
         in_n[e] = l < hi;
         // the table index: the shard token's position, or (per-shard
         // layout) the local token index itself
-        pos_n[e] = in_n[e] ? (a.local_tables ? l : (l / a.I) * DI + dI + l % a.I) : 0;
-        blk_n[e] = in_n[e] ? __ldg(trow + pos_n[e] / a.block_size) : -1;
+        const int32_t lq = fast_div(l, a.div_I);
+        pos_n[e] = in_n[e] ? (a.local_tables ? l : lq * DI + dI + (l - lq * a.I)) : 0;
+        blk_n[e] = in_n[e] ? __ldg(trow + fast_div(pos_n[e], a.div_bs)) : -1;
       }
     };
     // rows of the tile whose block ids are in in_n / pos_n / blk_n
@@ -444,7 +445,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(DecodeArgs a) {
       for (int e = 0; e < 2; ++e) {
         valid[e] = in_n[e] && blk_n[e] >= 0 && blk_n[e] < a.num_blocks;
         // cache row (fits in 31 bits: the library only takes caches of < 2^31 rows)
-        crow[e] = valid[e] ? blk_n[e] * a.block_size + pos_n[e] % a.block_size : 0;
+        crow[e] = valid[e] ? blk_n[e] * a.block_size + (pos_n[e] - fast_div(pos_n[e], a.div_bs) * a.block_size) : 0;
       }
       bad = (in_n[0] && !valid[0]) || (in_n[1] && !valid[1]);
     };

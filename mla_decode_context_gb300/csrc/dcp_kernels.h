@@ -9,6 +9,28 @@
 
 namespace dcp {
 
+// Division of a non-negative int32 n < 2^31 by a positive int32 d fixed for
+// a launch, as a multiply-high, an add and a shift (the round-up method of
+// Granlund and Montgomery, "Division by Invariant Integers using
+// Multiplication", PLDI 1994): with l = ceil(log2 d) and
+// m = floor(2^32 (2^l - d) / d) + 1 (which fits in 32 bits),
+// n / d = (umulhi(n, m) + n) >> l, the sum staying below 2^32.
+struct FastDiv {
+  uint32_t d, m, l;
+};
+inline FastDiv make_fastdiv(int32_t d) {
+  FastDiv f{static_cast<uint32_t>(d), 0u, 0u};
+  while ((1ull << f.l) < f.d) ++f.l;
+  f.m = static_cast<uint32_t>(((1ull << 32) * ((1ull << f.l) - f.d)) / f.d + 1);
+  return f;
+}
+#ifdef __CUDACC__
+__device__ __forceinline__ int32_t fast_div(int32_t n, const FastDiv& f) {
+  const uint32_t u = static_cast<uint32_t>(n);
+  return static_cast<int32_t>((__umulhi(u, f.m) + u) >> f.l);
+}
+#endif
+
 // Everything one decode launch needs (validated by the C ABI).
 struct DecodeArgs {
   const __nv_bfloat16* q;
@@ -31,6 +53,7 @@ struct DecodeArgs {
   const int32_t* seq_lens;
   const int32_t* qsl;
   int32_t B, T, H, max_seq_len, max_q_len, D, I;
+  FastDiv div_I, div_bs;  // division by I and by block_size (set with them)
   // the shards this launch computes: d0 .. d0 + Dn - 1 (all D on one GPU;
   // one per rank when each DCP rank holds only its own shard).  Outputs and
   // per-shard tables are indexed by d - d0.
