@@ -477,6 +477,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(DecodeArgs a) {
     bool ok = true;
     if (score) ok = __all_sync(0xffffffffu, mbar_wait(&bar.q_ready, 0));
     TR_LAP(1, 5);  // producers: waiting for Q to leave the stages
+    // slot j % nslots and the parity of j / nslots, kept as running values
+    // (nslots is 5 or 7 by CTA, so the compiler cannot fold the division)
+    int st = group, round = 0;
     for (int j = group; j < ntiles && ok; j += 2) {
       bool valid[2];
       int32_t crow[2];
@@ -504,12 +507,11 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(DecodeArgs a) {
         rows_of(valid, crow, bad);
         if (j + 2 < ntiles) fetch(j + 2);
       }
-      const int st = j % nslots;
       // the abort flag is read here and tested after this tile's copies are
       // issued, so that its shared-memory latency overlaps them
       const bool ab = aborted(bar);
       TR_LAP(1, 2);  // producers: block ids, loop
-      ok = __all_sync(0xffffffffu, mbar_wait(&own_free[st], ((j / nslots) & 1) ^ 1));
+      ok = __all_sync(0xffffffffu, mbar_wait(&own_free[st], (round & 1) ^ 1));
       TR_LAP(1, 0);  // producers: waiting for a free slot
       if (!ok) break;
       if (__any_sync(0xffffffffu, bad) && score && lane == 0) report(a.dev_error, DCP_DEVERR_BAD_BLOCK);
@@ -563,6 +565,11 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(DecodeArgs a) {
       if (__any_sync(0xffffffffu, ab)) {
         ok = false;
         break;
+      }
+      st += 2;
+      if (st >= nslots) {
+        st -= nslots;
+        ++round;
       }
     }
     if (!ok) set_abort(bar, a.dev_error);
