@@ -426,7 +426,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(DecodeArgs a) {
     const int nslots = score ? kStages : kOwn;
     const int32_t DI = a.D * a.I, dI = d * a.I;
     bool in_n[2] = {false, false};
-    int32_t pos_n[2] = {0, 0}, blk_n[2] = {-1, -1};
+    int32_t off_n[2] = {0, 0}, blk_n[2] = {-1, -1};  // row within its block, block id
     auto fetch = [&](int jj) {  // positions fit in 32 bits (seq_lens are int32)
 #pragma unroll
       for (int e = 0; e < 2; ++e) {
@@ -435,17 +435,19 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(DecodeArgs a) {
         // the table index: the shard token's position, or (per-shard
         // layout) the local token index itself
         const int32_t lq = fast_div(l, a.div_I);
-        pos_n[e] = in_n[e] ? (a.local_tables ? l : lq * DI + dI + (l - lq * a.I)) : 0;
-        blk_n[e] = in_n[e] ? __ldg(trow + fast_div(pos_n[e], a.div_bs)) : -1;
+        const int32_t pos = in_n[e] ? (a.local_tables ? l : lq * DI + dI + (l - lq * a.I)) : 0;
+        const int32_t pb = fast_div(pos, a.div_bs);
+        off_n[e] = pos - pb * a.block_size;
+        blk_n[e] = in_n[e] ? __ldg(trow + pb) : -1;
       }
     };
-    // rows of the tile whose block ids are in in_n / pos_n / blk_n
+    // rows of the tile whose block ids are in in_n / off_n / blk_n
     auto rows_of = [&](bool (&valid)[2], int32_t (&crow)[2], bool& bad) {
 #pragma unroll
       for (int e = 0; e < 2; ++e) {
         valid[e] = in_n[e] && blk_n[e] >= 0 && blk_n[e] < a.num_blocks;
         // cache row (fits in 31 bits: the library only takes caches of < 2^31 rows)
-        crow[e] = valid[e] ? blk_n[e] * a.block_size + (pos_n[e] - fast_div(pos_n[e], a.div_bs) * a.block_size) : 0;
+        crow[e] = valid[e] ? blk_n[e] * a.block_size + off_n[e] : 0;
       }
       bad = (in_n[0] && !valid[0]) || (in_n[1] && !valid[1]);
     };
