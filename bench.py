@@ -43,8 +43,8 @@ KV_ROW_BYTES = 576 * 2
 MEASURED_TRAFFIC = {
     "workload": "long_ctx_120k_b1_d8_i1",
     "source": "mla_decode_context_gb300/csrc/dcp_decode_tc.cu",
-    "sha256": "f7262c923063fb1717ec20e77ec97aa07ab3f4bae255fd4f00f4c51094e01cf8",
-    "bytes": 138479104 + 3334912,
+    "sha256": "01c328af7b842cc31264d00ef7af55146925e277e91ece86a5183da2a335c41a",
+    "bytes": 138475520 + 3714304,
 }
 
 
