@@ -612,10 +612,6 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(DecodeArgs a) {
       idle = moved ? 0u : idle + 1u;
       if (moved) TR_LAP(2, 1); else TR_LAP(2, 0);  // forwarder: working / polling
       if (idle > kWaitLimit) ok = false;
-      // an idle round backs off for a few tens of nanoseconds, so that the
-      // polls leave the issue slots of this SM sub-partition to the S
-      // issuers and softmax warps that share it
-      if (!moved) __nanosleep(32);
     }
     if (!ok) set_abort(bar, a.dev_error);
   } else if (!score && warp == 8) {
