@@ -40,6 +40,13 @@ SMALL = [
     # loads at once (its batched path)
     wl.DecodeSpec("h128_d1_32_splits", seed=42, B=1, seq_lens=(9000,), H=128, block_size=64, D=1,
                   interleave=1),
+    # head counts that leave TMEM lane quarters partly or wholly empty
+    wl.DecodeSpec("h1_d2_i1_single_head", seed=44, B=2, seq_lens=(700, 65), H=1, block_size=16, D=2,
+                  interleave=1),
+    wl.DecodeSpec("h33_d4_i2_odd_heads", seed=45, B=2, seq_lens=(1200, 3), q_len=2, H=33, block_size=32, D=4,
+                  interleave=2),
+    wl.DecodeSpec("h100_d8_i1_partial_quarter", seed=46, B=2, seq_lens=(2500, 90), H=100, block_size=64, D=8,
+                  interleave=1),
     # more units than clusters, so one split per shard: 20-25 tiles per unit
     # (every stage, S buffer and P slot reused several times)
     wl.DecodeSpec("h128_b12_unsplit", seed=39, B=12,
