@@ -249,10 +249,13 @@ __device__ __forceinline__ void set_abort(Bars& bar, int32_t* dev_error) {
 // Two FP8 E4M3 codes -> bf16x2 of code x s.  Exact: E4M3 values convert
 // exactly to half and to fp32, s is a power of two, and a code has at most 4
 // significant bits, so the product (in fp32 range) is exact in bf16 too.
-__device__ __forceinline__ uint32_t e4m3x2_to_bf16x2(uint32_t codes, float s) {
+// (s2: the scale in both halves of a packed fp32 pair; one f32x2 multiply.)
+__device__ __forceinline__ uint32_t e4m3x2_to_bf16x2(uint32_t codes, uint64_t s2) {
   const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(codes & 0xffffu), __NV_E4M3);
   const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&h));
-  __nv_bfloat162 b = __floats2bfloat162_rn(f.x * s, f.y * s);
+  float lo, hi;
+  f2_unpack(f2_mul(f2_pack(f.x, f.y), s2), lo, hi);
+  __nv_bfloat162 b = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&b);
 }
 
@@ -549,7 +552,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(DecodeArgs a) {
           if constexpr (kFp8) {
             // 8 codes -> 8 bf16 (zeros for rows that were not loaded)
             const uint2 w = cur[e][i];
-            const float sc = cur_scale[e];
+            const uint64_t sc = f2_pack(cur_scale[e], cur_scale[e]);
             const uint4 v = make_uint4(e4m3x2_to_bf16x2(w.x, sc), e4m3x2_to_bf16x2(w.x >> 16, sc),
                                        e4m3x2_to_bf16x2(w.y, sc), e4m3x2_to_bf16x2(w.y >> 16, sc));
             asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
