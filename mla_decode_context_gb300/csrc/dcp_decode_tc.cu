@@ -136,9 +136,9 @@ struct __align__(8) Bars {
   uint64_t fin_l;             // value: 1/l of every head arrived from the score CTA
   uint64_t fin[1 + kSParts * kSBuf];  // each issuing warp's MMAs complete
   uint64_t m_pub[8];          // score: running max after tile j posted (phase j / 8 of m_pub[j % 8]; 4 warps)
-  // score: the other group has read the max posted after tile k (phase k / 8
-  // of m_read[k % 8]; 4 warps): slot k % 8 may take tile k + 8's max
-  uint64_t m_read[8];
+  // score: how many of its tiles producer group g has claimed a stage for
+  // (written by the group's first warp, read by the other group)
+  int32_t claimed[2];
   uint64_t sm_fin;            // score: both softmax groups' final l and m written (8 warps)
   uint64_t never;             // test hook only: initialised, never arrived on
   // score: valid rows of tile j in mask[j % 16] (written by the producer
@@ -345,7 +345,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(DecodeArgs a) {
     mbar_init(&bar.o_final, 1);
     mbar_init(&bar.fin_l, 1);
     for (int i = 0; i < 1 + kSParts * kSBuf; ++i) mbar_init(&bar.fin[i], 1);
-    for (int i = 0; i < 8; ++i) { mbar_init(&bar.m_pub[i], 4); mbar_init(&bar.m_read[i], 4); }
+    for (int i = 0; i < 8; ++i) mbar_init(&bar.m_pub[i], 4);
+    bar.claimed[0] = bar.claimed[1] = 0;
     mbar_init(&bar.sm_fin, 8);
     mbar_init(&bar.never, 1);
     bar.abort = 0;
@@ -485,6 +486,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(DecodeArgs a) {
     // slot j % nslots and the parity of j / nslots, kept as running values
     // (nslots is 5 or 7 by CTA, so the compiler cannot fold the division)
     int st = group, round = 0;
+    // the other group's claim count, read a tile ahead of its test (below)
+    // so that the shared-memory load's latency overlaps a tile's work
+    int32_t other_claimed = 0;
     for (int j = group; j < ntiles && ok; j += 2) {
       bool valid[2];
       int32_t crow[2];
@@ -516,9 +520,21 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(DecodeArgs a) {
       // issued, so that its shared-memory latency overlaps them
       const bool ab = aborted(bar);
       TR_LAP(1, 2);  // producers: block ids, loop
-      ok = __all_sync(0xffffffffu, mbar_wait(&own_free[st], (round & 1) ^ 1));
+      // score CTA: the other group has claimed its stage for tile j - 5,
+      // which it did after S(j - 10) finished.  So the stage-free barrier
+      // below is at S(j - 5)'s phase or past it, and its parity can only
+      // mean S(j - 5), however the copies and MMAs of other tiles complete.
+      // (A monotonic count, not a parity wait: the groups may drift apart.)
+      if (score && j >= 5) {
+        const int32_t need = ((j - 5) >> 1) + 1;
+        for (uint32_t i = 0; other_claimed < need && i < kWaitLimit; ++i)
+          other_claimed = ld_relaxed_shared(&bar.claimed[group ^ 1]);
+        ok = __all_sync(0xffffffffu, other_claimed >= need);
+      }
+      ok = ok && __all_sync(0xffffffffu, mbar_wait(&own_free[st], (round & 1) ^ 1));
       TR_LAP(1, 0);  // producers: waiting for a free slot
       if (!ok) break;
+      if (score && gw == 0 && lane == 0) st_relaxed_shared(&bar.claimed[group], (j >> 1) + 1);
       if (__any_sync(0xffffffffu, bad) && score && lane == 0) report(a.dev_error, DCP_DEVERR_BAD_BLOCK);
       if (score) {
         // this warp's 8 rows of the tile's mask (lanes 8q .. 8q + 7 hold rows
@@ -571,6 +587,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(DecodeArgs a) {
         ok = false;
         break;
       }
+      if (score) other_claimed = ld_relaxed_shared(&bar.claimed[group ^ 1]);
       st += 2;
       if (st >= nslots) {
         st -= nslots;
@@ -744,19 +761,15 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(DecodeArgs a) {
     for (int j = sg; ok && j < ntiles; j += 2) {
       const int b = j % kSBuf, slot = j % kPSlots;
       // the other group's m after tile k, read early so that the load's
-      // latency overlaps the wait for S.  The read is acknowledged on
-      // m_read (except the first of the two reads of tile 0's max, at tile
-      // 1), and slot k % 8 takes tile k + 8's max only after that.
+      // latency overlaps the wait for S.  Its ring slot takes tile k + 8's
+      // max only after the writer has waited for this group's post of tile
+      // k + 5, which this group makes after this read.
       float m_other = -INFINITY;
       const int k = j == 1 ? 0 : j - 3;
       if (k >= 0) {
         ok = __all_sync(0xffffffffu, mbar_wait(&bar.m_pub[k & 7], (k >> 3) & 1));
         if (!ok) break;
         m_other = *reinterpret_cast<volatile float*>(&m_ring[(k & 7) * 128 + h]);
-        if (j != 1) {
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&bar.m_read[k & 7]);
-        }
       }
       TR_LAP(4, 0);  // softmax: the other group's max
       ok = __all_sync(0xffffffffu, mbar_wait(&bar.s_full[b], (j / kSBuf) & 1));
@@ -813,10 +826,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(DecodeArgs a) {
         if (m_used != -INFINITY) l_sum *= ex2_approx(m_used - tmax);
         m_used = tmax;
       }
-      if (j >= 8) {  // the other group has read tile j - 8's max from this slot
-        ok = __all_sync(0xffffffffu, mbar_wait(&bar.m_read[j & 7], ((j - 8) >> 3) & 1));
-        if (!ok) break;
-      }
+      // (tile j - 8's max, in this slot, was read at tile j - 5, before the
+      // other group posted tile j - 3's max, which this group waited for)
       m_ring[(j & 7) * 128 + h] = m_used;
       __syncwarp();
       if (lane == 0) mbar_arrive(&bar.m_pub[j & 7]);

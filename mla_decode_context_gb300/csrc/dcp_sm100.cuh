@@ -160,6 +160,17 @@ __device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity
   return false;
 }
 
+// Shared-memory int read and written as volatile (a progress count whose
+// readers only need to see it grow; shared memory holds no stale copies), so
+// that the compiler keeps each access but may still schedule the code
+// around it.
+__device__ __forceinline__ int32_t ld_relaxed_shared(const int32_t* p) {
+  return *reinterpret_cast<const volatile int32_t*>(p);
+}
+__device__ __forceinline__ void st_relaxed_shared(int32_t* p, int32_t v) {
+  *reinterpret_cast<volatile int32_t*>(p) = v;
+}
+
 // ---------------------------------------------------------------------------
 // proxies
 // ---------------------------------------------------------------------------
