@@ -43,8 +43,8 @@ KV_ROW_BYTES = 576 * 2
 MEASURED_TRAFFIC = {
     "workload": "long_ctx_120k_b1_d8_i1",
     "source": "mla_decode_context_gb300/csrc/dcp_decode_tc.cu",
-    "sha256": "01c328af7b842cc31264d00ef7af55146925e277e91ece86a5183da2a335c41a",
-    "bytes": 138475520 + 3714304,
+    "sha256": "de065022a661eab2239faaf65bfaacff79ba1fa1e0e32b6e477cb627a7b6897e",
+    "bytes": 138471680 + 3572224,
 }
 
 
