@@ -486,10 +486,24 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(DecodeArgs a) {
     // slot j % nslots and the parity of j / nslots, kept as running values
     // (nslots is 5 or 7 by CTA, so the compiler cannot fold the division)
     int st = group, round = 0;
-    // the other group's claim count, read a tile ahead of its test (below)
-    // so that the shared-memory load's latency overlaps a tile's work
+    // the other group's claim count as last read: it only grows, so it is
+    // read again only when it falls short of what a tile needs (below)
     int32_t other_claimed = 0;
     for (int j = group; j < ntiles && ok; j += 2) {
+      // score CTA: the other group has claimed its stage for tile j - 5,
+      // which it did after S(j - 10) finished.  So the stage-free barrier
+      // below is at S(j - 5)'s phase or past it, and its parity can only
+      // mean S(j - 5), however the copies and MMAs of other tiles complete.
+      // (A monotonic count, not a parity wait: the groups may drift apart.
+      // Tested first in the iteration, before this tile's global loads are
+      // issued, so that the shared-memory read does not queue behind them.)
+      if (score && j >= 5) {
+        const int32_t need = ((j - 5) >> 1) + 1;
+        for (uint32_t i = 0; other_claimed < need && i < kWaitLimit; ++i)
+          other_claimed = ld_relaxed_shared(&bar.claimed[group ^ 1]);
+        ok = __all_sync(0xffffffffu, other_claimed >= need);
+      }
+      if (!ok) break;
       bool valid[2];
       int32_t crow[2];
       bool bad;
@@ -520,17 +534,6 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(DecodeArgs a) {
       // issued, so that its shared-memory latency overlaps them
       const bool ab = aborted(bar);
       TR_LAP(1, 2);  // producers: block ids, loop
-      // score CTA: the other group has claimed its stage for tile j - 5,
-      // which it did after S(j - 10) finished.  So the stage-free barrier
-      // below is at S(j - 5)'s phase or past it, and its parity can only
-      // mean S(j - 5), however the copies and MMAs of other tiles complete.
-      // (A monotonic count, not a parity wait: the groups may drift apart.)
-      if (score && j >= 5) {
-        const int32_t need = ((j - 5) >> 1) + 1;
-        for (uint32_t i = 0; other_claimed < need && i < kWaitLimit; ++i)
-          other_claimed = ld_relaxed_shared(&bar.claimed[group ^ 1]);
-        ok = __all_sync(0xffffffffu, other_claimed >= need);
-      }
       ok = ok && __all_sync(0xffffffffu, mbar_wait(&own_free[st], (round & 1) ^ 1));
       TR_LAP(1, 0);  // producers: waiting for a free slot
       if (!ok) break;
@@ -587,7 +590,6 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(DecodeArgs a) {
         ok = false;
         break;
       }
-      if (score) other_claimed = ld_relaxed_shared(&bar.claimed[group ^ 1]);
       st += 2;
       if (st >= nslots) {
         st -= nslots;
