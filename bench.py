@@ -43,8 +43,8 @@ KV_ROW_BYTES = 576 * 2
 MEASURED_TRAFFIC = {
     "workload": "long_ctx_120k_b1_d8_i1",
     "source": "mla_decode_context_gb300/csrc/dcp_decode_tc.cu",
-    "sha256": "b5b0b42707728556ba04a2d63b80b45073bca8061c6a4c6ae519ed36d7ac71c3",
-    "bytes": 138473728 + 3651840,
+    "sha256": "8860f957253300ce238eda7d63bee12e7beb54440514f8c9108221a331460717",
+    "bytes": 138498816 + 3641344,
 }
 
 

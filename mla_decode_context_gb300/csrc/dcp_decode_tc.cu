@@ -164,6 +164,11 @@ static_assert(kSmemBytes <= 232448, "exceeds the 227 KB of shared memory per CTA
 __host__ __device__ constexpr int stage_chunk_off(int st, int c) { return kOffStages + st * kStageBytes + c * kChunkBytes; }
 static_assert(kPSlotBytes % 1024 == 0 && kOffP % 1024 == 0, "P tiles must sit on swizzle-atom boundaries");
 static_assert(kOffRecv + kRecv * kHalfBytes <= kOffP, "value CTA rings overlap the P slots");
+// The receive warp's p_ok arrival for tile j + kPSlots must not land in tile
+// j's phase: it waits for chunks 0-3 of that tile, whose receive slot is
+// refilled only after PV(j + kPSlots - kRecv), which is PV(j) or later only
+// when kRecv <= kPSlots.
+static_assert(kRecv <= kPSlots, "a receive ring deeper than the P slots lets p_ok phases mix tiles");
 
 // Cycle accounting for performance work, compiled only with -DDCP_TRACE=R
 // (never in the library build): the warps of role R (1 producers, 2 score
@@ -697,6 +702,12 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(DecodeArgs a) {
     const uint32_t id_s = idesc_bf16(128, kTile, 0, 0);
     const uint64_t dk = smem_desc(smem_base + kOffStages, 16, 1024, kSwizzle128B);
     const uint32_t dS = tbase + kColS + 96 * b + 32 * part;
+    // The part's first k-step: Q columns and the stage's chunk offset.  A
+    // tcgen05.mma holds its issuing thread for tens of cycles, and any
+    // arithmetic that the next one's operands wait for adds to that, so the
+    // operands of a chunk's four MMAs are its base plus constants.
+    const uint32_t qa = tbase + kColQ + 96 * part;
+    const uint64_t dkp = dk + static_cast<uint64_t>((3 * part * kChunkBytes) >> 4);
     bool ok = __all_sync(0xffffffffu, mbar_wait(&bar.q_ready, 0));
     tc_fence_after();
     TR_LAP(3, 5);
@@ -719,12 +730,14 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(DecodeArgs a) {
       if (part == 0 && lane == 0) mbar_arrive(&bar.s_full[b]);
       tc_fence_after();
       if (lane == 0) {
-        const uint64_t so = static_cast<uint64_t>((st * kStageBytes) >> 4);
-#pragma unroll 6
-        for (int i = 0; i < 12; ++i) {
-          const int k = 12 * part + i;
-          mma_ts(dS, tbase + kColQ + 8 * k, dk + so + (((k >> 2) * kChunkBytes + (k & 3) * 32) >> 4), id_s, i > 0);
+        uint64_t bc = dkp + static_cast<uint64_t>((st * kStageBytes) >> 4);
+        uint32_t ac = qa;
+#pragma unroll 1
+        for (int c = 0; c < 3; ++c, bc += kChunkBytes >> 4, ac += 32) {
+#pragma unroll
+          for (int i = 0; i < 4; ++i) mma_ts(dS, ac + 8 * i, bc + 2 * i, id_s, (c | i) != 0);
         }
+        TR_LAP(3, 3);  // S issuer: the 12 MMAs
         mma_commit(&bar.s_full[b]);
         mma_commit_mc(&bar.s_done[st], 0x3);
       }

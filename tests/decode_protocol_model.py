@@ -12,6 +12,9 @@ finishing, remote arrivals) delivered at a random later time.
 
 What a run checks:
   * no deadlock, and no arrival beyond a barrier's count;
+  * no phase completed by arrivals meant for different tiles (each arrival
+    names its tile; an early arrival for a later tile that lands in an
+    earlier tile's open phase would let that phase complete too soon);
   * no aliased wait: a parity wait never passes while its barrier is a phase
     behind the one it targets (the parity of phase t - 1 equals that of
     t + 1), nor is a wait left behind by two phases;
@@ -42,8 +45,15 @@ class Bar:
     def __init__(self, name, count):
         self.name, self.count = name, count
         self.pending, self.tx, self.done = count, 0, 0
+        self.tag = None         # the tile the open phase's arrivals are for
 
-    def arrive(self, n=1):
+    def arrive(self, n=1, tag=None):
+        if tag is not None:
+            if self.tag is None:
+                self.tag = tag
+            elif self.tag != tag:
+                raise ProtocolError("%s: phase %d mixes arrivals for tiles %s and %s"
+                                    % (self.name, self.done, self.tag, tag))
         self.pending -= n
         if self.pending < 0:
             raise ProtocolError("over-arrival on %s (phase %d)" % (self.name, self.done))
@@ -57,6 +67,7 @@ class Bar:
         if self.pending == 0 and self.tx == 0:
             self.done += 1
             self.pending = self.count
+            self.tag = None
 
 
 class Model:
@@ -199,9 +210,9 @@ class Model:
                 self.mask[j % 16] = dict(tile=j, read=False)
             yield ("do", write)
             # warp 0 arms the value CTA's 16 KB; warps 1-3 arrive
-            yield ("do", lambda st=st: (self.b(0, "kv_full", st).txop(HALF), self.b(0, "kv_full", st).arrive()))
+            yield ("do", lambda st=st, j=j: (self.b(0, "kv_full", st).txop(HALF), self.b(0, "kv_full", st).arrive(tag=j)))
             for _ in range(3):
-                yield ("do", lambda st=st: self.b(0, "kv_full", st).arrive())
+                yield ("do", lambda st=st, j=j: self.b(0, "kv_full", st).arrive(tag=j))
 
             def landed(j=j, st=st):
                 self.stage[st]["own"] = True
@@ -236,7 +247,7 @@ class Model:
                 self.check(self.stage[st]["tile"] == jf and self.stage[st]["own"],
                            "forwarder fenced stage %s for tile %s before its rows landed", st, jf)
                 if self.mut != "kv_full_without_fence":
-                    yield ("do", lambda st=st: self.b(0, "kv_full", st).arrive())
+                    yield ("do", lambda st=st, jf=jf: self.b(0, "kv_full", st).arrive(tag=jf))
                 jf += 1
                 moved = True
             if jc < jf and self.passed(0, "v_free", jc % K_RECV, jc // K_RECV - 1, "score fwd"):
@@ -285,11 +296,11 @@ class Model:
             st, vs, os_ = j % K_STAGES, j % K_RECV, j % K_OWN
             yield self.W(1, "v_full", vs, j // K_RECV)
 
-            def arrivals(st=st, vs=vs):
+            def arrivals(st=st, vs=vs, j=j):
                 self.b(1, "v_full", vs).txop(HALF)
                 self.b(1, "v_full", vs).arrive()
-                self.b(1, "s_done", st).arrive()
-                self.later(lambda: self.b(0, "s_done", st).arrive())
+                self.b(1, "s_done", st).arrive(tag=j)
+                self.later(lambda: self.b(0, "s_done", st).arrive(tag=j))
             yield ("do", arrivals)
             if self.mut != "recv_skips_own_rows":
                 yield self.W(1, "own_loaded", os_, j // K_OWN)
@@ -300,7 +311,7 @@ class Model:
                 if o["tile"] == j and o["landed"]:
                     o["fenced"] = True
             yield ("do", fence)
-            yield ("do", lambda slot=j % K_PSLOTS: self.b(1, "p_ok", slot).arrive())
+            yield ("do", lambda slot=j % K_PSLOTS, j=j: self.b(1, "p_ok", slot).arrive(tag=j))
 
     def s_issuer(self, b, part):
         yield self.W(0, "q_ready", 0, 0)
@@ -320,7 +331,7 @@ class Model:
                                b, j, sl["tile"])
                     self.sslot[b] = dict(tile=j, parts_done=0, read=False)
                 if part == 0:
-                    self.b(0, "s_full", b).arrive()
+                    self.b(0, "s_full", b).arrive(tag=j)
 
                 def done():
                     sl2 = self.sslot[b]
@@ -328,9 +339,9 @@ class Model:
                                j, part, b, sl2["tile"])
                     sl2["parts_done"] += 1
                     self.stage[st]["s_done"].add(part)
-                    self.b(0, "s_full", b).arrive()
-                    self.b(0, "s_done", st).arrive()
-                    self.b(1, "s_done", st).arrive()
+                    self.b(0, "s_full", b).arrive(tag=j)
+                    self.b(0, "s_done", st).arrive(tag=j)
+                    self.b(1, "s_done", st).arrive(tag=j)
                 self.later(done, fifo=("S", b, part))
             yield ("do", issue)
 
@@ -358,7 +369,7 @@ class Model:
                 sl["read"] = True
             yield ("do", read_s)
             for _ in range(4):
-                yield ("do", lambda b=b: self.b(0, "s_free", b).arrive())
+                yield ("do", lambda b=b, j=j: self.b(0, "s_free", b).arrive(tag=j))
 
             def post(j=j):
                 m = self.mring[j % 8]
@@ -368,7 +379,7 @@ class Model:
                 self.mring[j % 8] = dict(tile=j, reads_left=len(readers))
             yield ("do", post)
             for _ in range(4):
-                yield ("do", lambda j=j: self.b(0, "m_pub", j % 8).arrive())
+                yield ("do", lambda j=j: self.b(0, "m_pub", j % 8).arrive(tag=j))
             if self.mut != "softmax_skips_p_free":
                 yield self.W(0, "p_free", slot, j // K_PSLOTS - 1)
 
@@ -413,7 +424,7 @@ class Model:
                                                       "O rescaled before PV(%s) finished", jp))
             m_prev_set = True
             for _ in range(4):
-                yield ("do", lambda slot=slot: self.b(1, "p_ok", slot).arrive())
+                yield ("do", lambda slot=slot, j=j: self.b(1, "p_ok", slot).arrive(tag=j))
 
     def pv_issuer(self):
         for j in range(self.n):

@@ -24,3 +24,32 @@ def test_planted_protocol_mistake_is_caught(mutation):
             except M.ProtocolError:
                 return
     pytest.fail("no interleaving exposed the planted mistake %r" % mutation)
+
+
+@pytest.mark.parametrize("own,recv", [(8, 3), (9, 2)])
+def test_other_splits_of_the_value_rings_hold(monkeypatch, own, recv):
+    # the value CTA's own and receive rings share one region; the kernel's
+    # split is 7 + 4, and these fit the same region
+    monkeypatch.setattr(M, "K_OWN", own)
+    monkeypatch.setattr(M, "K_RECV", recv)
+    for ntiles in (1, 2, 5, 9, 16, 23, 54):
+        for seed in range(15):
+            M.run(ntiles, seed)
+
+
+def test_receive_ring_deeper_than_the_p_slots_is_caught(monkeypatch):
+    # With more receive slots than P slots, the receive warp's p_ok arrival
+    # for tile j + 4 can land in tile j's open phase (its receive slot no
+    # longer waits for PV(j)), so PV(j) could start before O is rescaled for
+    # tile j.  A build with these ring sizes gave wrong outputs on the GPU;
+    # the kernel now asserts kRecv <= kPSlots at compile time.
+    monkeypatch.setattr(M, "K_OWN", 6)
+    monkeypatch.setattr(M, "K_RECV", 5)
+    for ntiles in (6, 9, 17, 54):
+        for seed in range(40):
+            try:
+                M.run(ntiles, seed)
+            except M.ProtocolError as e:
+                assert "mixes arrivals" in str(e)
+                return
+    pytest.fail("the early p_ok arrival was not caught")
