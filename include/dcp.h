@@ -279,8 +279,13 @@ dcp_status_t dcp_mla_decode_partial_local(
  *                   block_size, 576] and kv_scale fp32 [num_blocks,
  *                   block_size] (required, else DCP_ERR_INVALID_ARG); the
  *                   latent value of a slot is code x scale.  Other values:
- *                   DCP_ERR_UNSUPPORTED_DTYPE.  The fp8 form runs on the
- *                   CUDA-core kernel.
+ *                   DCP_ERR_UNSUPPORTED_DTYPE.  The tensor-core kernel
+ *                   (H <= 128) widens each code x scale to bf16 on its way
+ *                   into shared memory (the fp32 product, rounded to
+ *                   nearest even): exact when the scale is a power of two,
+ *                   else one bf16 rounding of each latent value, as a bf16
+ *                   cache holds them.  The CUDA-core kernel applies the
+ *                   scale in fp32 to the dot products and the PV weights.
  *   per_shard_tables, bt_shard_stride, shard_begin, shard_count
  *                   0: one table row per request ([B, bt_width]); 1:
  *                   per-shard tables as for dcp_mla_decode_partial_local.

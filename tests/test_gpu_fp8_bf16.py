@@ -87,6 +87,29 @@ def test_fp8_walker_bit_exact(spec, kernel):
     PC.check(O.cpu().numpy(), lse.cpu().numpy(), n, E, "%s/%s" % (spec.name, kernel))
 
 
+@pytest.mark.parametrize("spec", [FP8[0], FP8[1], FP8[3]], ids=lambda s: s.name)
+def test_fp8_scales_that_are_not_powers_of_two(spec, kernel):
+    """Any fp32 scale: the CUDA-core kernel applies it in fp32 and matches the
+    oracle on the codes and scales; the tensor-core kernel widens each
+    code x scale to bf16 (the fp32 product, rounded to nearest even), so it
+    matches the oracle run on the bf16 cache that holds exactly those
+    values."""
+    inp = wl.make_decode_inputs(spec)
+    rng = np.random.default_rng(spec.seed + 1000)
+    factor = rng.uniform(0.55, 0.95, size=inp["kv_scale"].shape)
+    inp["kv_scale"] = (inp["kv_scale"].astype(np.float64) * factor).astype(np.float32)
+    t = G.to_device(inp)
+    O, lse, err = _decode(inp, t)
+    assert err == 0
+    ref = inp
+    if kernel == "tc":
+        widened = oracle.fp8_e4m3_to_f64(inp["kv_cache"]).astype(np.float32) * inp["kv_scale"][..., None]
+        ref = dict(inp, kv_dtype="bf16", kv_cache=wl.f32_to_bf16_bits(widened))
+        del ref["kv_scale"]
+    O_ref, lse_ref, _ = oracle.decode_partial(ref)
+    G.check_partials(O.cpu().numpy(), lse.cpu().numpy(), O_ref, lse_ref, "%s/%s" % (spec.name, kernel))
+
+
 BF16_OUT = [
     wl.DecodeSpec("bf16out_h128_d8", seed=151, B=3, seq_lens=(1, 700, 2049), H=128, block_size=64, D=8, interleave=1),
     wl.DecodeSpec("bf16out_long_split", seed=152, B=1, seq_lens=(9000,), H=128, block_size=64, D=8, interleave=1),
