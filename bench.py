@@ -43,8 +43,8 @@ KV_ROW_BYTES = 576 * 2
 MEASURED_TRAFFIC = {
     "workload": "long_ctx_120k_b1_d8_i1",
     "source": "mla_decode_context_gb300/csrc/dcp_decode_tc.cu",
-    "sha256": "8860f957253300ce238eda7d63bee12e7beb54440514f8c9108221a331460717",
-    "bytes": 138498816 + 3641344,
+    "sha256": "91603822c8091e51eff03f02e74802a5b06dd511a7ff12e9339098457043c685",
+    "bytes": 138472192 + 3473920,
 }
 
 

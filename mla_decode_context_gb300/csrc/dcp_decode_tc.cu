@@ -42,8 +42,10 @@
 // interleave); rows that must not be read (past the split, bad block ids)
 // are zero-filled.  (TMA boxes were measured to cost a few hundred cycles
 // of issue each, and the shard-strided rows of small interleaves allow only
-// 8-row boxes, which capped the stream well below HBM bandwidth; a single
-// SM's cp.async stream tops out near 16 B/clk, hence the split.)
+// 8-row boxes, which capped the stream well below HBM bandwidth.  One SM's
+// cp.async stream could carry whole rows, but the score CTA loading every
+// chunk itself measured no faster on long contexts and slower on batched
+// ones, hence the split.)
 //
 // Warp roles (736 threads):
 //   warps 0-3   score: Q load, then softmax group 0 (thread = head = TMEM
