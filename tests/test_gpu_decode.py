@@ -47,6 +47,19 @@ SMALL = [
                   interleave=2),
     wl.DecodeSpec("h100_d8_i1_partial_quarter", seed=46, B=2, seq_lens=(2500, 90), H=100, block_size=64, D=8,
                   interleave=1),
+    # verification widths: 8 rows a request (the widest run side by side in
+    # the unit order), mixed widths that still group by 4 across requests,
+    # and 9 rows (no grouping), with a block size and an interleave that are
+    # not powers of two
+    wl.DecodeSpec("h128_q8_rows_innermost", seed=47, B=3, seq_lens=(9, 1500, 3000), q_len=8, H=128, block_size=64,
+                  D=8, interleave=1),
+    wl.DecodeSpec("h128_mixed_q_group4", seed=48, B=4, seq_lens=(700, 5, 2000, 64), q_len=(4, 2, 2, 4), H=128,
+                  block_size=64, D=4, interleave=2),
+    wl.DecodeSpec("h64_q9_bs48_i5", seed=49, B=3, seq_lens=(400, 20, 1000), q_len=(9, 1, 5), H=64, block_size=48,
+                  D=4, interleave=5),
+    # shard lengths on tile and split edges (32, 256, 257 tokens a shard)
+    wl.DecodeSpec("h128_tile_edges_bs80", seed=50, B=4, seq_lens=(128, 1024, 1028, 1027), H=128, block_size=80,
+                  D=4, interleave=1, extra_rows=1),
     # more units than clusters, so one split per shard: 20-25 tiles per unit
     # (every stage, S buffer and P slot reused several times)
     wl.DecodeSpec("h128_b12_unsplit", seed=39, B=12,

@@ -8,8 +8,9 @@ partial must equal the oracle's, exactly.  Geometries: the 120,000-token
 long-context workload at full size (D=8, interleave 1, nine splits per
 shard), the batched workload's geometry at full size (64 requests,
 interleave 64 = block size, permuted table), the largest shard count (32),
-an interleave that does not divide the block size (3), and verification rows
-with causal offsets and padding requests."""
+an interleave that does not divide the block size (3), block sizes and an
+interleave that are not powers of two, and verification rows with causal
+offsets and padding requests."""
 import numpy as np
 import pytest
 import torch
@@ -30,6 +31,12 @@ GEOMETRIES = [
                   block_size=64, D=8, interleave=1, extra_rows=2),
     wl.DecodeSpec("exact_d2_i16_bs32_long", seed=64, B=1, seq_lens=(40000,), H=128, block_size=32, D=2,
                   interleave=16),
+    # divisors that are not powers of two (the walker divides by the
+    # interleave and the block size with precomputed multipliers)
+    wl.DecodeSpec("exact_d4_i5_bs48", seed=65, B=3, seq_lens=(7001, 20, 1000), q_len=(3, 1, 2), H=64, block_size=48,
+                  D=4, interleave=5),
+    wl.DecodeSpec("exact_d8_i1_bs80", seed=66, B=2, seq_lens=(20000, 1027), H=128, block_size=80, D=8,
+                  interleave=1),
 ]
 
 
