@@ -188,7 +188,8 @@ __global__ void __launch_bounds__(256, 1) rate_lanes(int W, int L, int iters, lo
 
 // Six unrolled issuers (warps 0-5, N = 32, own accumulators) next to K noise
 // warps (warps 8 .. 8 + K - 1) doing kind `noise` until the issuers are done.
-__global__ void __launch_bounds__(768, 1) rate_noise(int noise, int K, int iters, const uint4* gbuf, size_t gwords,
+__global__ void __launch_bounds__(768, 1) rate_noise(int noise, int K, int W, int spread, int iters, const uint4* gbuf,
+                                                     size_t gwords,
                                                      long long* cyc, int* err) {
   extern __shared__ __align__(1024) unsigned char sm[];
   __shared__ uint32_t tslot;
@@ -199,7 +200,7 @@ __global__ void __launch_bounds__(768, 1) rate_noise(int noise, int K, int iters
   unsigned char* bsm = sm + pad;               // B operand: 32 KB
   unsigned char* scratch = bsm + 49152;        // noise: 16 warps x 4 KB
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  for (int i = threadIdx.x; i < 32768 / 4; i += blockDim.x) reinterpret_cast<uint32_t*>(bsm)[i] = 0x3c003c00u;
+  for (int i = threadIdx.x; i < 36864 / 4; i += blockDim.x) reinterpret_cast<uint32_t*>(bsm)[i] = 0x3c003c00u;
   if (threadIdx.x == 0) {
     for (int i = 0; i < 8; ++i) asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(su32(&done[i])) : "memory");
     asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(su32(&never)) : "memory");
@@ -227,11 +228,13 @@ __global__ void __launch_bounds__(768, 1) rate_noise(int noise, int K, int iters
   __syncthreads();
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
   if (warp < 6) {
-    if (lane == 0) {
+    if (lane == 0 && warp < W) {
       const uint32_t id = idesc(128, 32);
       const uint32_t d = tbase + static_cast<uint32_t>(warp * 32);
       const uint32_t a0 = tbase + 256u;
       const uint64_t bd0 = sdesc(su32(bsm));
+      uint64_t bc = bd0;  // spread: the chunk of this group of four k-steps (nine 4 KB chunks, as a stage)
+      int c = 0;
       long long t0 = clock64();
       for (int i = 0; i < iters; i += 4) {
 #pragma unroll
@@ -240,8 +243,12 @@ __global__ void __launch_bounds__(768, 1) rate_noise(int noise, int K, int iters
           asm volatile(
               "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
               "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d),
-              "r"(a0 + k * 8u), "l"(bd0 + 2u * k), "r"(id), "r"(acc)
+              "r"(a0 + k * 8u), "l"(bc + 2u * k), "r"(id), "r"(acc)
               : "memory");
+        }
+        if (spread) {
+          bc += 4096 >> 4;
+          if (++c == 9) { c = 0; bc = bd0; }
         }
       }
       long long t1 = clock64();
@@ -266,7 +273,7 @@ __global__ void __launch_bounds__(768, 1) rate_noise(int noise, int K, int iters
     const uint4* gsrc = gbuf + blockIdx.x * span;
     size_t g = static_cast<size_t>((warp - 8) * 512 + lane);
     uint32_t sink = 0;
-    for (uint32_t it = 0; it < (1u << 22) && finished < 6; ++it) {
+    for (uint32_t it = 0; it < (1u << 22) && finished < W; ++it) {
       if (noise == 0) {  // non-blocking mbarrier polls
         uint32_t r;
         asm volatile(
@@ -410,7 +417,7 @@ int main() {
       for (int K : {0, 4, 8, 16}) {
         if (K == 0 && noise > 0) continue;
         for (int rep = 0; rep < 2; ++rep)
-          rate_noise<<<sms, 768, smem2>>>(noise, K, iters, gbuf, gbytes / 16, cyc, err);
+          rate_noise<<<sms, 768, smem2>>>(noise, K, 6, 0, iters, gbuf, gbytes / 16, cyc, err);
         cudaError_t e = cudaDeviceSynchronize();
         std::vector<long long> h(sms * 16);
         cudaMemcpy(h.data(), cyc, h.size() * sizeof(long long), cudaMemcpyDeviceToHost);
@@ -425,6 +432,26 @@ int main() {
                K ? kinds[noise] : "nothing", issue[issue.size() / 2] / iters, issue[issue.size() / 2] / iters / 6,
                cudaGetErrorString(e));
       }
+    // B read from nine distinct 4 KB chunks (36 KB, as the decode's stage)
+    // rather than one: W issuers, with or without cp.async streams
+    for (int W : {3, 6})
+      for (int spread : {0, 1})
+        for (int K : {0, 8, 16}) {
+          for (int rep = 0; rep < 2; ++rep)
+            rate_noise<<<sms, 768, smem2>>>(2, K, W, spread, iters, gbuf, gbytes / 16, cyc, err);
+          cudaError_t e = cudaDeviceSynchronize();
+          std::vector<long long> h(sms * 16);
+          cudaMemcpy(h.data(), cyc, h.size() * sizeof(long long), cudaMemcpyDeviceToHost);
+          std::vector<double> issue;
+          for (int b = 0; b < sms; ++b) {
+            long long mi = 0;
+            for (int q = 0; q < W; ++q) mi = std::max(mi, h[(b * 8 + q) * 2 + 0]);
+            issue.push_back(static_cast<double>(mi));
+          }
+          std::sort(issue.begin(), issue.end());
+          printf("%d issuers, B from %s, %2d cp.async warps: %7.1f cycles per MMA of one issuer %s\n", W,
+                 spread ? "9 chunks" : "1 chunk ", K, issue[issue.size() / 2] / iters, cudaGetErrorString(e));
+        }
     cudaFree(gbuf);
   }
   int herr = 0;
