@@ -43,8 +43,8 @@ KV_ROW_BYTES = 576 * 2
 MEASURED_TRAFFIC = {
     "workload": "long_ctx_120k_b1_d8_i1",
     "source": "mla_decode_context_gb300/csrc/dcp_decode_tc.cu",
-    "sha256": "91603822c8091e51eff03f02e74802a5b06dd511a7ff12e9339098457043c685",
-    "bytes": 138472192 + 3473920,
+    "sha256": "21f0c8784680f1d9fb1d5b4f941b2b19c6e6731e1204f219a0727fa435dda605",
+    "bytes": 138472704 + 3266304,
 }
 
 

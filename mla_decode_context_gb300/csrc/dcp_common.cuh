@@ -54,12 +54,21 @@ struct RequestOfRow {
   int32_t seq;     // seq_lens[b]
 };
 
+// width_hint > 0: a guess of the rows per request (requests of equal width
+// from row 0), whose entries are read together with the bounds, so that the
+// common case costs one round of loads instead of two; the guess is used
+// only when qsl confirms it.
 __device__ __forceinline__ RequestOfRow request_of_row(const int32_t* __restrict__ seq_lens,
-                                                       const int32_t* __restrict__ qsl, int32_t B, int32_t r) {
+                                                       const int32_t* __restrict__ qsl, int32_t B, int32_t r,
+                                                       int32_t width_hint = 0) {
   RequestOfRow q{-1, 0, 0, 0};
   if (B <= 0) return q;
+  const int32_t gh = width_hint > 0 ? min(max(r, 0) / width_hint, B - 1) : 0;
   const int32_t qa = __ldg(qsl), qn = __ldg(qsl + 1), qB = __ldg(qsl + B);
+  int32_t hlo = 0, hhi = 0, hsq = 0;
+  if (width_hint > 0) hlo = __ldg(qsl + gh), hhi = __ldg(qsl + gh + 1), hsq = __ldg(seq_lens + gh);
   if (r < qa || r >= qB) return q;
+  if (width_hint > 0 && hlo <= r && r < hhi) return RequestOfRow{gh, hlo, hhi, hsq};
   const int32_t step = qn - qa;
   if (step > 0) {
     const int32_t g = (r - qa) / step;
@@ -91,7 +100,7 @@ __device__ __forceinline__ RowInfo resolve_row(const int32_t* __restrict__ seq_l
                                                const int32_t* __restrict__ qsl, int32_t B,
                                                int32_t r, int32_t max_seq_len, int32_t max_q_len) {
   RowInfo ri{-1, 0, true, 0u};
-  const RequestOfRow q = request_of_row(seq_lens, qsl, B, r);
+  const RequestOfRow q = request_of_row(seq_lens, qsl, B, r, max_q_len);
   if (q.b < 0) return ri;
   ri.b = q.b;
   int32_t seq = q.seq;

@@ -287,6 +287,23 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(DecodeArgs a) {
   const int d = a.d0 + uc.dd;  // shard (of D)
   const int s = uc.s;
 
+  if (score && warp < 8) {
+    // Q load, issued first (it depends only on the row) so that its latency
+    // overlaps the row lookup's loads and the set-up.  The 147 KB of Q (128
+    // heads x 576 dims, the same for every unit of a row) come in with one
+    // round of cp.async into stages 0-3 (unused until Q is in TMEM): head h
+    // at 1152 h, its 16-byte unit u at position u ^ (h & 7) within each
+    // 8-unit group.  Heads h >= H are zero.
+    const unsigned char* qb = reinterpret_cast<const unsigned char*>(a.q + static_cast<int64_t>(r) * a.q_stride_tok);
+    const uint32_t qs = smem_u32(smem) + kOffStages;
+    for (int p = threadIdx.x; p < 128 * 72; p += 256) {
+      const int hh = p / 72, u = p - hh * 72;
+      const int us = (u & ~7) | ((u & 7) ^ (hh & 7));
+      cp_async16_zfill(qs + hh * 1152 + us * 16, qb + (hh < a.H ? hh : 0) * 1152 + u * 16, hh < a.H ? 16u : 0u);
+    }
+    cp_async_commit();
+  }
+
   const RowInfo ri = resolve_row(a.seq_lens, a.qsl, a.B, r, a.max_seq_len, a.max_q_len);
   if (ri.err && threadIdx.x == 0 && cta == 0 && d == a.d0 && s == 0) report(a.dev_error, ri.err);
   const int32_t n_local = ri.padding ? 0 : local_len(ri.L, d, a.D, a.I);
@@ -296,6 +313,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(DecodeArgs a) {
   const int64_t pair0 = ((static_cast<int64_t>(s) * a.Dn + (d - a.d0)) * a.T + r) * a.H;
 
   if (ntiles == 0) {
+    if (score && warp < 8) cp_async_wait<0>();  // the Q copies land before the CTA leaves
     // empty shard / split or padding row: masked at the source, no KV read
     if (warp < 4) {
       const int h = threadIdx.x;
@@ -314,24 +332,11 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(DecodeArgs a) {
     return;
   }
 
-  if (score && warp < 8) {
-    // Q load, issued before the set-up below so that its latency overlaps
-    // it.  The 147 KB of Q (128 heads x 576 dims, the same for every unit of
-    // a row) come in with one round of cp.async into stages 0-3 (unused until
-    // Q is in TMEM): head h at 1152 h, its 16-byte unit u at position
-    // u ^ (h & 7) within each 8-unit group.  Heads h >= H are zero.
-    const unsigned char* qb = reinterpret_cast<const unsigned char*>(a.q + static_cast<int64_t>(r) * a.q_stride_tok);
-    const uint32_t qs = smem_u32(smem) + kOffStages;
-    for (int p = threadIdx.x; p < 128 * 72; p += 256) {
-      const int hh = p / 72, u = p - hh * 72;
-      const int us = (u & ~7) | ((u & 7) ^ (hh & 7));
-      cp_async16_zfill(qs + hh * 1152 + us * 16, qb + (hh < a.H ? hh : 0) * 1152 + u * 16, hh < a.H ? 16u : 0u);
-    }
-    cp_async_commit();
-  }
 
   // ---------------------------------------------------------------- setup
-  if (threadIdx.x == 0) {
+  // (by a thread of a warp that issued no Q copies, so that the barrier
+  // stores do not queue behind its own)
+  if (threadIdx.x == 32 * kProdWarp0) {
     for (int i = 0; i < kStages; ++i) {
       mbar_init(&bar.kv_loaded[i], kGroupThreads);
       mbar_init(&bar.kv_full[i], 5);  // 4 producer warps of the tile's group + the forwarder
