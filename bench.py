@@ -719,9 +719,9 @@ def main(argv=None):
                     help="only call the standalone combine on one sweep point (for ncu captures)")
     ap.add_argument("--headline-only", action="store_true",
                     help="skip the other workloads and the combine sweep")
-    ap.add_argument("--probe", choices=["mma_rate", "load_rate", "tma_rate"],
+    ap.add_argument("--probe", choices=["mma_rate", "load_rate", "tma_rate", "store_rate"],
                     help="build and run one stand-alone hardware-rate probe (tensor-core issue rate, "
-                         "cp.async streaming rate, TMA streaming rate) instead of the bench")
+                         "cp.async streaming rate, TMA streaming rate, store rate) instead of the bench")
     args = ap.parse_args(argv)
     if args.probe:
         return run_probe(args.probe)

@@ -82,7 +82,7 @@ def build(verbose: bool = False, force: bool = False, ptxas_info: bool = False) 
     return LIB
 
 
-PROBES = ("mma_rate", "load_rate", "tma_rate")
+PROBES = ("mma_rate", "load_rate", "tma_rate", "store_rate")
 
 
 def build_probe(name: str) -> str:
