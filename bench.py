@@ -43,8 +43,8 @@ KV_ROW_BYTES = 576 * 2
 MEASURED_TRAFFIC = {
     "workload": "long_ctx_120k_b1_d8_i1",
     "source": "mla_decode_context_gb300/csrc/dcp_decode_tc.cu",
-    "sha256": "21f0c8784680f1d9fb1d5b4f941b2b19c6e6731e1204f219a0727fa435dda605",
-    "bytes": 138472704 + 3266304,
+    "sha256": "3e06e1d4a1ac77e1264b21130289797621bb4514db15edb1ef54dfc5c6e444d5",
+    "bytes": 138473472 + 3628032,
 }
 
 

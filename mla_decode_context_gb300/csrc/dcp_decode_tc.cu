@@ -19,16 +19,20 @@
 // (P and the max go from score to value), so neither waits on a round trip to
 // the other inside the tile loop.
 //
-// Each tile is read from HBM once, half by each CTA: the score CTA loads
-// chunks 0-3 and the rope chunk 8 (20 KB) into its stage ring, the value CTA
-// chunks 4-7 (16 KB) into its "own" ring, with 16-byte cp.async, one shard
-// token per row, straight into the 128B-swizzled chunk-major layout the MMAs
-// read.  Each CTA forwards the 16 KB its peer lacks with one DSMEM bulk copy:
-// value -> score chunks 4-7 (into the stage, which then holds the whole tile
-// for S), score -> value chunks 0-3 (into a 4-slot receive ring; PV reads V
-// from the receive slot and the own slot).  A DSMEM copy was measured at
-// ~900 cycles of round trip plus ~47 cycles per KB, so each direction carries
-// at most 24 KB per tile.
+// Each tile is read from HBM once.  The score CTA loads chunks 0-3 and the
+// rope chunk 8 (20 KB) into its stage ring, the value CTA chunks 4-7 (16 KB)
+// into its "own" ring, with 16-byte cp.async, one shard token per row,
+// straight into the 128B-swizzled chunk-major layout the MMAs read; the value
+// CTA forwards chunks 4-7 into the score CTA's stage with one DSMEM bulk copy,
+// so the stage holds the whole tile for S.  PV reads V from the own slot and
+// a 4-slot receive ring that holds chunks 0-3:
+//   bf16 cache: the value CTA's warps 19-22 (idle otherwise) load them from
+//     L2 (the score CTA has just read the same lines) with cp.async, so the
+//     score SM sends nothing back and its stage is free once S is done;
+//   fp8 cache: the score CTA copies its widened chunks 0-3 over (one DSMEM
+//     bulk copy), as the value CTA would otherwise widen the codes twice.
+// A DSMEM copy was measured at ~900 cycles of round trip plus ~47 cycles per
+// KB, so each direction carries at most 24 KB per tile.
 //
 // While an SM streams cp.async, its shared-memory loads, proxy fences and
 // st.async take ~500 cycles each and a release-ordered remote arrival
@@ -59,11 +63,13 @@
 //                      ring -> score stage); 9 receive-ring arrivals and
 //                      the own slot's proxy fence for PV
 //   warp 10     both:  TMEM allocation; score: proxy fence of the stage's
-//                      own rows, forwarder (stage -> receive ring); value:
-//                      PV issuer
+//                      own rows, forwarder (fp8: stage -> receive ring);
+//                      value: PV issuer
 //   warps 11-18 both:  producers (cp.async; the score CTA's wait until Q has
 //                      left stages 0-3 for TMEM)
 //   warps 19-22 score: softmax group 1 (odd tiles)
+//               value: bf16 cache: receive-ring producers (chunks 0-3 of
+//                      every tile)
 // Every wait is bounded (a timeout sets DCP_DEVERR_TIMEOUT and ends the unit).
 #include "dcp_kernels.h"
 #include "dcp_sm100.cuh"
@@ -115,13 +121,18 @@ struct __align__(8) Bars {
   // own rows visible to the tensor cores
   uint64_t kv_full[kStages];
   // s_done (both CTAs): the score CTA's stage of tile j is free again: all
-  // three parts of S(j) done and chunks 0-3 of tile j have landed in the
-  // value CTA
+  // three parts of S(j) done (fp8: and chunks 0-3 of tile j have landed in
+  // the value CTA)
   uint64_t s_done[kStages];
   uint64_t own_loaded[kOwn];    // value: rows of tile j in own slot j % kOwn (every thread of its producer group)
   uint64_t own_free[kOwn];      // value: PV(j) done with own slot j % kOwn
-  uint64_t v_full[kRecv];       // value: chunks 0-3 of tile j landed in receive slot j % kRecv
-  uint64_t v_free[kRecv];       // score (multicast commit of PV(j)): receive slot j % kRecv may refill
+  // value: chunks 0-3 of tile j landed in receive slot j % kRecv (bf16: every
+  // thread of the receive-ring producers; fp8: the score CTA's copy)
+  uint64_t v_full[kRecv];
+  // both (multicast commit of PV(j)): receive slot j % kRecv may refill
+  // (bf16: the value CTA's receive-ring producers wait; fp8: the score CTA's
+  // forwarder)
+  uint64_t v_free[kRecv];
   uint64_t s_full[kSBuf];     // score: the three parts' commits + part 0's arrival
   uint64_t s_free[kSBuf];     // score: the softmax has read the slot (4 warps)
   uint64_t q_staged;          // score: Q is in shared memory (threads of warps 0-7)
@@ -340,10 +351,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(DecodeArgs a) {
     for (int i = 0; i < kStages; ++i) {
       mbar_init(&bar.kv_loaded[i], kGroupThreads);
       mbar_init(&bar.kv_full[i], 5);  // 4 producer warps of the tile's group + the forwarder
-      mbar_init(&bar.s_done[i], kSParts + 1);
+      mbar_init(&bar.s_done[i], kFp8 ? kSParts + 1 : kSParts);
     }
     for (int i = 0; i < kOwn; ++i) { mbar_init(&bar.own_loaded[i], kGroupThreads); mbar_init(&bar.own_free[i], 1); }
-    for (int i = 0; i < kRecv; ++i) { mbar_init(&bar.v_full[i], 1); mbar_init(&bar.v_free[i], 1); }
+    for (int i = 0; i < kRecv; ++i) { mbar_init(&bar.v_full[i], kFp8 ? 1 : kGroupThreads); mbar_init(&bar.v_free[i], 1); }
     for (int i = 0; i < kSBuf; ++i) { mbar_init(&bar.s_full[i], kSParts + 1); mbar_init(&bar.s_free[i], 4); }
     mbar_init(&bar.q_staged, 256);
     mbar_init(&bar.q_ready, 8);
@@ -366,7 +377,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(DecodeArgs a) {
     if (!score) {
       // every P slot starts free: expect the first P tile and max column
       for (int i = 0; i < kPSlots; ++i) mbar_arrive_expect_tx(&bar.p_full[i], kPTx);
-      for (int i = 0; i < kRecv; ++i) mbar_arrive_expect_tx(&bar.v_full[i], kHalfBytes);
+      if (kFp8)
+        for (int i = 0; i < kRecv; ++i) mbar_arrive_expect_tx(&bar.v_full[i], kHalfBytes);
       mbar_arrive_expect_tx(&bar.fin_l, 128 * 4);
     }
   }
@@ -416,7 +428,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(DecodeArgs a) {
   const uint32_t smem_base = smem_u32(smem);
   int pdone = 0;  // value, warps 0-3: P tiles received
 
-  if (warp >= kProdWarp0 && warp < kSmWarp1) {
+  if ((warp >= kProdWarp0 && warp < kSmWarp1) || (!kFp8 && !score && warp >= kSmWarp1)) {
     // ----------------------------------------------------------- producers
     // Two groups of four warps take alternate tiles (a producer thread's
     // issue is latency-bound, so two tiles are in flight at once).  Warp gw
@@ -437,9 +449,14 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(DecodeArgs a) {
     const int row0 = 8 * gw + (lane >> 3), row1 = row0 + 4;
     const int nch = score ? 5 : 4;  // chunks this CTA loads itself
     const unsigned char* kvb = reinterpret_cast<const unsigned char*>(a.kv);
-    uint64_t* own_free = score ? bar.s_done : bar.own_free;
-    uint64_t* own_loaded = score ? bar.kv_loaded : bar.own_loaded;
-    const int nslots = score ? kStages : kOwn;
+    // bf16 cache, value CTA: group 2 (warps 19-22) loads chunks 0-3 of every
+    // tile into the receive ring, one tile after another; groups 0 and 1 take
+    // alternate tiles' chunks 4-7 as in the score CTA
+    const bool vrecv = !kFp8 && !score && group == 2;
+    const int step = vrecv ? 1 : 2, j0 = vrecv ? 0 : group;
+    uint64_t* own_free = score ? bar.s_done : (vrecv ? bar.v_free : bar.own_free);
+    uint64_t* own_loaded = score ? bar.kv_loaded : (vrecv ? bar.v_full : bar.own_loaded);
+    const int nslots = score ? kStages : (vrecv ? kRecv : kOwn);
     const int32_t DI = a.D * a.I, dI = d * a.I;
     bool in_n[2] = {false, false};
     int32_t off_n[2] = {0, 0}, blk_n[2] = {-1, -1};  // row within its block, block id
@@ -486,7 +503,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(DecodeArgs a) {
     bool valid_n[2] = {false, false};
     int32_t crow_n[2] = {0, 0};
     bool bad_n = false;
-    fetch(group);
+    fetch(j0);
     if constexpr (kFp8) {
       rows_of(valid_n, crow_n, bad_n);
       load_codes(valid_n, crow_n);
@@ -497,11 +514,11 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(DecodeArgs a) {
     TR_LAP(1, 5);  // producers: waiting for Q to leave the stages
     // slot j % nslots and the parity of j / nslots, kept as running values
     // (nslots is 5 or 7 by CTA, so the compiler cannot fold the division)
-    int st = group, round = 0;
+    int st = j0, round = 0;
     // the other group's claim count as last read: it only grows, so it is
     // read again only when it falls short of what a tile needs (below)
     int32_t other_claimed = 0;
-    for (int j = group; j < ntiles && ok; j += 2) {
+    for (int j = j0; j < ntiles && ok; j += step) {
       // score CTA: the other group has claimed its stage for tile j - 5,
       // which it did after S(j - 10) finished.  So the stage-free barrier
       // below is at S(j - 5)'s phase or past it, and its parity can only
@@ -540,7 +557,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(DecodeArgs a) {
         }
       } else {
         rows_of(valid, crow, bad);
-        if (j + 2 < ntiles) fetch(j + 2);
+        if (j + step < ntiles) fetch(j + step);
       }
       // the abort flag is read here and tested after this tile's copies are
       // issued, so that its shared-memory latency overlaps them
@@ -576,10 +593,11 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(DecodeArgs a) {
 #pragma unroll
         for (int i = 0; i < nch; ++i) {
           // score: chunks 0-3, 8 at stage_chunk_off(st, c); value: chunks
-          // 4-7 at its own slot's chunk offsets 0-3
-          const int c = score ? (i < 4 ? i : 8) : 4 + i;
+          // 4-7 at its own slot's chunk offsets 0-3, or (receive-ring
+          // producers) chunks 0-3 at the receive slot's
+          const int c = score ? (i < 4 ? i : 8) : (vrecv ? i : 4 + i);
           const uint32_t dst = score ? smem_base + stage_chunk_off(st, c) + swz
-                                     : smem_base + kOffOwn + st * kHalfBytes + i * kChunkBytes + swz;
+                                     : smem_base + (vrecv ? kOffRecv : kOffOwn) + st * kHalfBytes + i * kChunkBytes + swz;
           if constexpr (kFp8) {
             // 8 codes -> 8 bf16 (zeros for rows that were not loaded)
             const uint2 w = cur[e][i];
@@ -602,7 +620,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(DecodeArgs a) {
         ok = false;
         break;
       }
-      st += 2;
+      st += step;
       if (st >= nslots) {
         st -= nslots;
         ++round;
@@ -616,8 +634,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(DecodeArgs a) {
     // true (non-blocking polls), so that neither waits behind the other:
     //   fence: once this CTA's own rows of tile jf have landed, fence them
     //          into the async proxy and arrive on kv_full (for S);
-    //   copy:  once tile jc < jf is fenced and the value CTA's receive slot
-    //          is free, copy chunks 0-3 (16 KB) into it.
+    //   copy:  (fp8) once tile jc < jf is fenced and the value CTA's receive
+    //          slot is free, copy chunks 0-3 (16 KB) into it.  (bf16: the
+    //          value CTA loads them itself; jc follows jf.)
     // (kv_loaded(jf + 5) needs S(jf), hence the fence of jf: no parity
     // aliasing.)  The loop gives up after kWaitLimit polls without progress.
     bool ok = __all_sync(0xffffffffu, mbar_wait(&bar.q_ready, 0));
@@ -634,7 +653,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(DecodeArgs a) {
         ++jf;
         moved = true;
       }
-      if (jc < jf && __all_sync(0xffffffffu, mbar_peek_cluster(&bar.v_free[jc % kRecv], ((jc / kRecv) & 1) ^ 1))) {
+      if (!kFp8) jc = jf;
+      if (kFp8 && jc < jf && __all_sync(0xffffffffu, mbar_peek_cluster(&bar.v_free[jc % kRecv], ((jc / kRecv) & 1) ^ 1))) {
         const int st = jc % kStages, rs = jc % kRecv;
         if (lane == 0)  // chunks 0-3 of the stage -> the receive slot
           bulk_copy_to_peer(map_peer(smem_base + kOffRecv + rs * kHalfBytes, peer), smem + stage_chunk_off(st, 0),
@@ -671,12 +691,13 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(DecodeArgs a) {
     if (!ok) set_abort(bar, a.dev_error);
   } else if (!score && warp == 9) {
     // ------------------------------------------------- receive-ring arrivals
-    // When tile j's chunks 0-3 land, re-arm the slot for tile j + kRecv (that
-    // fill needs PV(j) first, so it cannot complete before this) and tell
-    // both CTAs that the score CTA's stage of tile j has been read (a relaxed
-    // arrival: the copy's reads are complete, and nothing written here needs
-    // publishing).  Then, once this CTA's own rows of tile j have landed,
-    // fence them into the async proxy and let PV(j) go.  (This warp's arrival
+    // When tile j's chunks 0-3 land (fp8: copied in), re-arm the slot for
+    // tile j + kRecv (that fill needs PV(j) first, so it cannot complete
+    // before this) and tell both CTAs that the score CTA's stage of tile j
+    // has been read (a relaxed arrival: the copy's reads are complete, and
+    // nothing written here needs publishing).  Then, once this CTA's own
+    // rows of tile j have landed, fence them (bf16: and the receive slot's
+    // rows) into the async proxy and let PV(j) go.  (This warp's arrival
     // for tile j + kPSlots needs v_full(j + kPSlots), hence PV(j) done, so it
     // cannot land in tile j's phase of p_ok.)
     bool ok = true;
@@ -685,7 +706,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(DecodeArgs a) {
       ok = __all_sync(0xffffffffu, mbar_wait_cluster(&bar.v_full[vs], (j / kRecv) & 1));
       TR_LAP(7, 0);  // receive warp: waiting for chunks 0-3
       if (!ok) break;
-      if (lane == 0) {
+      if (kFp8 && lane == 0) {
         mbar_arrive_expect_tx(&bar.v_full[vs], kHalfBytes);
         mbar_arrive(&bar.s_done[st]);
         mbar_arrive_remote_relaxed(map_peer(smem_u32(&bar.s_done[st]), peer));
@@ -694,7 +715,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(DecodeArgs a) {
       ok = __all_sync(0xffffffffu, mbar_wait(&bar.own_loaded[os], (j / kOwn) & 1));
       TR_LAP(7, 2);  // receive warp: waiting for own rows
       if (!ok) break;
-      fence_proxy_async_smem();  // the own slot's cp.async rows -> PV
+      fence_proxy_async_smem();  // the own (bf16: and receive) slot's cp.async rows -> PV
       __syncwarp();
       if (lane == 0) mbar_arrive(&bar.p_ok[j % kPSlots]);
       TR_LAP(7, 3);  // receive warp: fence

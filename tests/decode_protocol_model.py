@@ -10,6 +10,14 @@ parities and ring sizes, role by role) and runs it under random
 interleavings, with every asynchronous completion (copies landing, MMAs
 finishing, remote arrivals) delivered at a random later time.
 
+Two forms of the protocol, as the kernel has them:
+  * bf16 cache (``self_recv=True``): the value CTA loads chunks 0-3 of every
+    tile into its receive ring with its own producer group (group 2), so the
+    score CTA's stage is free once S is done;
+  * fp8 cache (``self_recv=False``): the score CTA's forwarder copies chunks
+    0-3 of each tile into the value CTA's receive ring, and the stage is free
+    once that copy has landed too.
+
 What a run checks:
   * no deadlock, and no arrival beyond a barrier's count;
   * no phase completed by arrivals meant for different tiles (each arrival
@@ -71,10 +79,11 @@ class Bar:
 
 
 class Model:
-    def __init__(self, ntiles, seed, rescale_prob=0.3, mutation=None):
+    def __init__(self, ntiles, seed, rescale_prob=0.3, mutation=None, self_recv=True):
         # `mutation` plants one mistake in the protocol (for the tests that
         # show the checks catch it): see MUTATIONS
         self.mut = mutation
+        self.self_recv = self_recv
         self.n = ntiles
         self.rng = random.Random(seed)
         self.rescale_prob = rescale_prob
@@ -87,7 +96,7 @@ class Model:
         self.stage = [dict(tile=None, own=False, fwd=False, s_done=set(), cp_read=True)
                       for _ in range(K_STAGES)]
         self.own = [dict(tile=None, landed=False, fwd_read=True, pv_read=True, fenced=False) for _ in range(K_OWN)]
-        self.recv = [dict(tile=None, landed=False, pv_read=True) for _ in range(K_RECV)]
+        self.recv = [dict(tile=None, landed=False, pv_read=True, fenced=False) for _ in range(K_RECV)]
         self.pslot = [dict(tile=None, bytes=0, pv_read=True, max_read=True) for _ in range(K_PSLOTS)]
         self.stg = [dict(tile=None, reads_left=0) for _ in range(K_PSLOTS)]
         self.sslot = [dict(tile=None, parts_done=0, read=True) for _ in range(K_SBUF)]
@@ -104,10 +113,10 @@ class Model:
         for cta in (0, 1):
             mk(cta, "kv_loaded", K_STAGES, 128)
             mk(cta, "kv_full", K_STAGES, 4 if self.mut == "kv_full_without_fence" else 5)
-            mk(cta, "s_done", K_STAGES, K_SPARTS + 1)
+            mk(cta, "s_done", K_STAGES, K_SPARTS if self.self_recv else K_SPARTS + 1)
             mk(cta, "own_loaded", K_OWN, 128)
             mk(cta, "own_free", K_OWN, 1)
-            mk(cta, "v_full", K_RECV, 1)
+            mk(cta, "v_full", K_RECV, 128 if self.self_recv else 1)
             mk(cta, "v_free", K_RECV, 1)
             mk(cta, "s_full", K_SBUF, K_SPARTS + 1)
             mk(cta, "s_free", K_SBUF, 4)
@@ -125,9 +134,10 @@ class Model:
         for i in range(K_PSLOTS):
             self.b(1, "p_full", i).txop(PTX)
             self.b(1, "p_full", i).arrive()
-        for i in range(K_RECV):
-            self.b(1, "v_full", i).txop(HALF)
-            self.b(1, "v_full", i).arrive()
+        if not self.self_recv:
+            for i in range(K_RECV):
+                self.b(1, "v_full", i).txop(HALF)
+                self.b(1, "v_full", i).arrive()
         self.b(1, "fin_l", 0).txop(128 * 4)
         self.b(1, "fin_l", 0).arrive()
 
@@ -141,7 +151,7 @@ class Model:
             self.check(len(s["s_done"]) == K_SPARTS,
                        "%s overwrote stage %s (tile %s) before S(%s) finished", who, st, j, s["tile"])
             self.check(s["cp_read"], "%s overwrote stage %s (tile %s) before tile %s's chunks 0-3 were copied", who, st, j, s["tile"])
-        self.stage[st] = dict(tile=j, own=False, fwd=False, s_done=set(), cp_read=False)
+        self.stage[st] = dict(tile=j, own=False, fwd=False, s_done=set(), cp_read=self.self_recv)
 
     def _delay(self):
         # heavy-tailed: most completions are quick, a few take very long
@@ -236,6 +246,25 @@ class Model:
                 self.b(1, "own_loaded", os_).arrive(128)
             yield ("do", lambda f=landed: self.later(f))
 
+    def value_recv_producers(self):
+        """bf16: the value CTA's group 2 loads chunks 0-3 of every tile into
+        receive slot j % K_RECV once PV(j - K_RECV) has freed it."""
+        for j in range(self.n):
+            vs = j % K_RECV
+            if self.mut != "recv_producers_skip_slot_free":
+                yield self.W(1, "v_free", vs, j // K_RECV - 1)
+
+            def write(j=j, vs=vs):
+                r = self.recv[vs]
+                self.check(r["pv_read"], "receive slot %s overwritten (tile %s) before PV(%s)", vs, j, r["tile"])
+                self.recv[vs] = dict(tile=j, landed=False, pv_read=False, fenced=False)
+            yield ("do", write)
+
+            def landed(j=j, vs=vs):
+                self.recv[vs]["landed"] = True
+                self.b(1, "v_full", vs).arrive(128)
+            yield ("do", lambda f=landed: self.later(f))
+
     def score_forwarder(self):
         yield self.W(0, "q_ready", 0, 0)
         yield ("do", lambda: self.later(lambda: self.b(1, "q_gone", 0).arrive()))
@@ -250,14 +279,16 @@ class Model:
                     yield ("do", lambda st=st, jf=jf: self.b(0, "kv_full", st).arrive(tag=jf))
                 jf += 1
                 moved = True
-            if jc < jf and self.passed(0, "v_free", jc % K_RECV, jc // K_RECV - 1, "score fwd"):
+            if self.self_recv:
+                jc = jf     # bf16: no copies; the forwarder only fences
+            elif jc < jf and self.passed(0, "v_free", jc % K_RECV, jc // K_RECV - 1, "score fwd"):
                 st, rs, j = jc % K_STAGES, jc % K_RECV, jc
 
                 def copy(st=st, rs=rs, j=j):
                     r = self.recv[rs]
                     self.check(r["pv_read"], "receive slot %s overwritten (tile %s) before PV(%s)", rs, j, r["tile"])
                     self.check(self.stage[st]["tile"] == j, "copy of tile %s from a stage holding %s", j, self.stage[st]["tile"])
-                    self.recv[rs] = dict(tile=j, landed=False, pv_read=False)
+                    self.recv[rs] = dict(tile=j, landed=False, pv_read=False, fenced=True)
 
                     def land():
                         self.stage[st]["cp_read"] = True
@@ -294,22 +325,28 @@ class Model:
     def recv_warp(self):
         for j in range(self.n):
             st, vs, os_ = j % K_STAGES, j % K_RECV, j % K_OWN
-            yield self.W(1, "v_full", vs, j // K_RECV)
+            if not (self.self_recv and self.mut == "recv_skips_v_full"):
+                yield self.W(1, "v_full", vs, j // K_RECV)
 
             def arrivals(st=st, vs=vs, j=j):
                 self.b(1, "v_full", vs).txop(HALF)
                 self.b(1, "v_full", vs).arrive()
                 self.b(1, "s_done", st).arrive(tag=j)
                 self.later(lambda: self.b(0, "s_done", st).arrive(tag=j))
-            yield ("do", arrivals)
+            if not self.self_recv:
+                yield ("do", arrivals)
             if self.mut != "recv_skips_own_rows":
                 yield self.W(1, "own_loaded", os_, j // K_OWN)
 
-            def fence(j=j, os_=os_):
-                # the proxy fence that makes the own slot's copies visible to PV
+            def fence(j=j, os_=os_, vs=vs):
+                # the proxy fence that makes the own slot's copies (and, bf16,
+                # the receive slot's) visible to PV
                 o = self.own[os_]
                 if o["tile"] == j and o["landed"]:
                     o["fenced"] = True
+                r = self.recv[vs]
+                if self.self_recv and r["tile"] == j and r["landed"]:
+                    r["fenced"] = True
             yield ("do", fence)
             yield ("do", lambda slot=j % K_PSLOTS, j=j: self.b(1, "p_ok", slot).arrive(tag=j))
 
@@ -434,8 +471,8 @@ class Model:
             def issue(j=j, vs=vs, os_=os_, slot=slot):
                 self.check(self.pslot[slot]["tile"] == j and self.pslot[slot]["bytes"] == PTX,
                            "PV(%s) issued before P landed", j)
-                self.check(self.recv[vs]["tile"] == j and self.recv[vs]["landed"],
-                           "PV(%s) issued before chunks 0-3 landed", j)
+                self.check(self.recv[vs]["tile"] == j and self.recv[vs]["landed"] and self.recv[vs]["fenced"],
+                           "PV(%s) issued before chunks 0-3 landed (and, loaded by cp.async, were fenced)", j)
                 self.check(self.own[os_]["tile"] == j and self.own[os_]["landed"] and self.own[os_]["fenced"],
                            "PV(%s) issued before chunks 4-7 landed and were fenced", j)
 
@@ -481,6 +518,8 @@ class Model:
             roles["sp%d" % g] = self.score_producers(g)
             roles["vp%d" % g] = self.value_producers(g)
             roles["sm%d" % g] = self.softmax(g)
+        if self.self_recv:
+            roles["vp2"] = self.value_recv_producers()
         for b in range(K_SBUF):
             for p in range(K_SPARTS):
                 roles["s%d%d" % (b, p)] = self.s_issuer(b, p)
@@ -552,9 +591,11 @@ class Model:
             # a passed wait needs nothing more; a "yield" lets the polling role retry
 
 
-MUTATIONS = ("producers_uncoupled", "kv_full_without_fence", "producers_skip_stage_free", "issuers_skip_s_free",
-             "softmax_skips_m_pub", "softmax_skips_p_free", "recv_skips_own_rows")
+# planted mistakes, and the protocol form each applies to (None: both)
+MUTATIONS = {"producers_uncoupled": None, "kv_full_without_fence": None, "producers_skip_stage_free": None,
+             "issuers_skip_s_free": None, "softmax_skips_m_pub": None, "softmax_skips_p_free": None,
+             "recv_skips_own_rows": None, "recv_producers_skip_slot_free": True, "recv_skips_v_full": True}
 
 
-def run(ntiles, seed, mutation=None):
-    Model(ntiles, seed, mutation=mutation).run()
+def run(ntiles, seed, mutation=None, self_recv=True):
+    Model(ntiles, seed, mutation=mutation, self_recv=self_recv).run()
