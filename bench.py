@@ -43,8 +43,8 @@ KV_ROW_BYTES = 576 * 2
 MEASURED_TRAFFIC = {
     "workload": "long_ctx_120k_b1_d8_i1",
     "source": "mla_decode_context_gb300/csrc/dcp_decode_tc.cu",
-    "sha256": "3e06e1d4a1ac77e1264b21130289797621bb4514db15edb1ef54dfc5c6e444d5",
-    "bytes": 138473472 + 3628032,
+    "sha256": "b201b4f053abdd1da9cc1496dd66c9790436a005f19d792309a54d3321f617e1",
+    "bytes": 138486016 + 3622400,
 }
 
 

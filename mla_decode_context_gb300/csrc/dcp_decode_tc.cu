@@ -19,18 +19,19 @@
 // (P and the max go from score to value), so neither waits on a round trip to
 // the other inside the tile loop.
 //
-// Each tile is read from HBM once.  The score CTA loads chunks 0-3 and the
-// rope chunk 8 (20 KB) into its stage ring, the value CTA chunks 4-7 (16 KB)
-// into its "own" ring, with 16-byte cp.async, one shard token per row,
-// straight into the 128B-swizzled chunk-major layout the MMAs read; the value
-// CTA forwards chunks 4-7 into the score CTA's stage with one DSMEM bulk copy,
-// so the stage holds the whole tile for S.  PV reads V from the own slot and
-// a 4-slot receive ring that holds chunks 0-3:
-//   bf16 cache: the value CTA's warps 19-22 (idle otherwise) load them from
-//     L2 (the score CTA has just read the same lines) with cp.async, so the
-//     score SM sends nothing back and its stage is free once S is done;
-//   fp8 cache: the score CTA copies its widened chunks 0-3 over (one DSMEM
-//     bulk copy), as the value CTA would otherwise widen the codes twice.
+// Each tile is read from HBM once, with 16-byte cp.async, one shard token
+// per row, straight into the 128B-swizzled chunk-major layout the MMAs read.
+// The score CTA's stage ring holds the whole tile for S; the value CTA holds
+// V in a 7-slot "own" ring (chunks 4-7) and a 4-slot receive ring (chunks
+// 0-3):
+//   bf16 cache: each CTA loads what it needs, the second read of a line
+//     hitting L2 (DRAM bytes stay 1.01x the tile bytes): the score CTA all
+//     nine chunks (36 KB), the value CTA chunks 4-7 with its producers and
+//     chunks 0-3 with its warps 19-22 (idle otherwise).  Only P crosses the
+//     cluster, so neither CTA's ring waits on the other's loads;
+//   fp8 cache: the codes are widened once, by the CTA that loads them: the
+//     score CTA loads chunks 0-3 and 8, the value CTA chunks 4-7, and each
+//     forwards the widened 16 KB its peer lacks with one DSMEM bulk copy.
 // A DSMEM copy was measured at ~900 cycles of round trip plus ~47 cycles per
 // KB, so each direction carries at most 24 KB per tile.
 //
@@ -59,8 +60,8 @@
 //                      third k of S for tiles j = i mod 2 into S slot i (a
 //                      tcgen05.mma holds its issuing thread far longer than
 //                      an N=32 product takes, so issue is spread over warps)
-//               value: 4-7 epilogue columns 256-511; 8 forwarder (own
-//                      ring -> score stage); 9 receive-ring arrivals and
+//               value: 4-7 epilogue columns 256-511; 8 forwarder (fp8:
+//                      own ring -> score stage); 9 receive-ring arrivals and
 //                      the own slot's proxy fence for PV
 //   warp 10     both:  TMEM allocation; score: proxy fence of the stage's
 //                      own rows, forwarder (fp8: stage -> receive ring);
@@ -115,10 +116,10 @@ constexpr uint32_t kTmemCols = 512;
 
 struct __align__(8) Bars {
   uint64_t kv_loaded[kStages];  // score: own rows of tile j landed (every thread of tile j's producer group)
-  // kv_full (score): the whole tile j is in its stage for S: the value CTA's
-  // 16 KB landed (armed by a producer), the four producer warps of the tile
-  // wrote their bytes of its row mask, and the forwarder has made this CTA's
-  // own rows visible to the tensor cores
+  // kv_full (score): the whole tile j is in its stage for S: (fp8) the value
+  // CTA's 16 KB landed (armed by a producer), the four producer warps of the
+  // tile wrote their bytes of its row mask, and the forwarder has made this
+  // CTA's own rows visible to the tensor cores
   uint64_t kv_full[kStages];
   // s_done (both CTAs): the score CTA's stage of tile j is free again: all
   // three parts of S(j) done (fp8: and chunks 0-3 of tile j have landed in
@@ -137,7 +138,7 @@ struct __align__(8) Bars {
   uint64_t s_free[kSBuf];     // score: the softmax has read the slot (4 warps)
   uint64_t q_staged;          // score: Q is in shared memory (threads of warps 0-7)
   uint64_t q_ready;           // score: Q is in TMEM and stages 0-3 are free again (warps 0-7)
-  uint64_t q_gone;            // value: the score CTA's stages no longer hold Q (remote arrival)
+  uint64_t q_gone;            // value (fp8): the score CTA's stages no longer hold Q (remote arrival)
   uint64_t p_full[kPSlots];   // value: P(j) and the max of tile j arrived
   uint64_t p_free[kPSlots];   // both (multicast commit of PV(j)); the score CTA waits on it
   // p_ok (value): PV(j) may go: the max is checked and O rescaled if needed
@@ -447,7 +448,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(DecodeArgs a) {
     const int gw = (warp - kProdWarp0) & 3;
     const int x = lane & 7;
     const int row0 = 8 * gw + (lane >> 3), row1 = row0 + 4;
-    const int nch = score ? 5 : 4;  // chunks this CTA loads itself
+    const int nch = score ? (kFp8 ? 5 : 9) : 4;  // chunks this CTA loads itself
     const unsigned char* kvb = reinterpret_cast<const unsigned char*>(a.kv);
     // bf16 cache, value CTA: group 2 (warps 19-22) loads chunks 0-3 of every
     // tile into the receive ring, one tile after another; groups 0 and 1 take
@@ -580,7 +581,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(DecodeArgs a) {
 #pragma unroll
           for (int q = 0; q < 4; ++q) m8 |= (((v0 >> (8 * q)) & 1u) << q) | (((v1 >> (8 * q)) & 1u) << (4 + q));
           reinterpret_cast<volatile uint8_t*>(&bar.mask[j & 15])[gw] = static_cast<uint8_t>(m8);
-          if (gw == 0) mbar_arrive_expect_tx(&bar.kv_full[st], kHalfBytes);
+          if (kFp8 && gw == 0) mbar_arrive_expect_tx(&bar.kv_full[st], kHalfBytes);
           else mbar_arrive(&bar.kv_full[st]);
         }
       }
@@ -592,10 +593,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(DecodeArgs a) {
         const uint32_t swz = static_cast<uint32_t>(row * 128 + ((x ^ (row & 7)) << 4));
 #pragma unroll
         for (int i = 0; i < nch; ++i) {
-          // score: chunks 0-3, 8 at stage_chunk_off(st, c); value: chunks
-          // 4-7 at its own slot's chunk offsets 0-3, or (receive-ring
-          // producers) chunks 0-3 at the receive slot's
-          const int c = score ? (i < 4 ? i : 8) : (vrecv ? i : 4 + i);
+          // score: chunks 0-8 (fp8: 0-3, 8) at stage_chunk_off(st, c);
+          // value: chunks 4-7 at its own slot's chunk offsets 0-3, or
+          // (receive-ring producers) chunks 0-3 at the receive slot's
+          const int c = score ? (kFp8 ? (i < 4 ? i : 8) : i) : (vrecv ? i : 4 + i);
           const uint32_t dst = score ? smem_base + stage_chunk_off(st, c) + swz
                                      : smem_base + (vrecv ? kOffRecv : kOffOwn) + st * kHalfBytes + i * kChunkBytes + swz;
           if constexpr (kFp8) {
@@ -640,8 +641,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(DecodeArgs a) {
     // (kv_loaded(jf + 5) needs S(jf), hence the fence of jf: no parity
     // aliasing.)  The loop gives up after kWaitLimit polls without progress.
     bool ok = __all_sync(0xffffffffu, mbar_wait(&bar.q_ready, 0));
-    // the value CTA's forwards into the stages (which held Q) may start
-    if (ok && lane == 0) mbar_arrive_remote(map_peer(smem_u32(&bar.q_gone), peer));
+    // fp8: the value CTA's forwards into the stages (which held Q) may start
+    if (kFp8 && ok && lane == 0) mbar_arrive_remote(map_peer(smem_u32(&bar.q_gone), peer));
     int jf = 0, jc = 0;
     uint32_t idle = 0;
     while (ok && jc < ntiles) {
@@ -670,11 +671,12 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(DecodeArgs a) {
     if (!ok) set_abort(bar, a.dev_error);
   } else if (!score && warp == 8) {
     // ------------------------------------------------- value CTA forwarder
-    // Own slot j % kOwn (chunks 4-7) -> the score CTA's stage of tile j, once
-    // that stage is free (tile j - 5 done there) and no longer holds Q.
-    bool ok = __all_sync(0xffffffffu, mbar_wait_cluster(&bar.q_gone, 0));
+    // fp8: own slot j % kOwn (chunks 4-7) -> the score CTA's stage of tile j,
+    // once that stage is free (tile j - 5 done there) and no longer holds Q.
+    // (bf16: the score CTA loads those chunks itself.)
+    bool ok = !kFp8 || __all_sync(0xffffffffu, mbar_wait_cluster(&bar.q_gone, 0));
     TR_LAP(6, 5);
-    for (int j = 0; j < ntiles && ok; ++j) {
+    for (int j = 0; kFp8 && j < ntiles && ok; ++j) {
       const int st = j % kStages, os = j % kOwn;
       ok = __all_sync(0xffffffffu, mbar_wait(&bar.own_loaded[os], (j / kOwn) & 1));
       TR_LAP(6, 0);  // value forwarder: waiting for own rows

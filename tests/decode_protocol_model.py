@@ -11,12 +11,14 @@ interleavings, with every asynchronous completion (copies landing, MMAs
 finishing, remote arrivals) delivered at a random later time.
 
 Two forms of the protocol, as the kernel has them:
-  * bf16 cache (``self_recv=True``): the value CTA loads chunks 0-3 of every
-    tile into its receive ring with its own producer group (group 2), so the
-    score CTA's stage is free once S is done;
-  * fp8 cache (``self_recv=False``): the score CTA's forwarder copies chunks
-    0-3 of each tile into the value CTA's receive ring, and the stage is free
-    once that copy has landed too.
+  * bf16 cache (``decoupled=True``): each CTA loads what it needs: the score
+    CTA the whole tile into its stage, the value CTA chunks 4-7 into its own
+    ring and (group 2) chunks 0-3 into its receive ring.  Only P crosses the
+    cluster, and a stage is free once S is done;
+  * fp8 cache (``decoupled=False``): the score CTA loads chunks 0-3 and 8,
+    the value CTA chunks 4-7, and each copies the 16 KB its peer lacks: the
+    value CTA's forwarder into the score CTA's stage, the score CTA's
+    forwarder into the value CTA's receive ring.
 
 What a run checks:
   * no deadlock, and no arrival beyond a barrier's count;
@@ -79,11 +81,11 @@ class Bar:
 
 
 class Model:
-    def __init__(self, ntiles, seed, rescale_prob=0.3, mutation=None, self_recv=True):
+    def __init__(self, ntiles, seed, rescale_prob=0.3, mutation=None, decoupled=True):
         # `mutation` plants one mistake in the protocol (for the tests that
         # show the checks catch it): see MUTATIONS
         self.mut = mutation
-        self.self_recv = self_recv
+        self.decoupled = decoupled
         self.n = ntiles
         self.rng = random.Random(seed)
         self.rescale_prob = rescale_prob
@@ -113,10 +115,10 @@ class Model:
         for cta in (0, 1):
             mk(cta, "kv_loaded", K_STAGES, 128)
             mk(cta, "kv_full", K_STAGES, 4 if self.mut == "kv_full_without_fence" else 5)
-            mk(cta, "s_done", K_STAGES, K_SPARTS if self.self_recv else K_SPARTS + 1)
+            mk(cta, "s_done", K_STAGES, K_SPARTS if self.decoupled else K_SPARTS + 1)
             mk(cta, "own_loaded", K_OWN, 128)
             mk(cta, "own_free", K_OWN, 1)
-            mk(cta, "v_full", K_RECV, 128 if self.self_recv else 1)
+            mk(cta, "v_full", K_RECV, 128 if self.decoupled else 1)
             mk(cta, "v_free", K_RECV, 1)
             mk(cta, "s_full", K_SBUF, K_SPARTS + 1)
             mk(cta, "s_free", K_SBUF, 4)
@@ -134,7 +136,7 @@ class Model:
         for i in range(K_PSLOTS):
             self.b(1, "p_full", i).txop(PTX)
             self.b(1, "p_full", i).arrive()
-        if not self.self_recv:
+        if not self.decoupled:
             for i in range(K_RECV):
                 self.b(1, "v_full", i).txop(HALF)
                 self.b(1, "v_full", i).arrive()
@@ -151,7 +153,7 @@ class Model:
             self.check(len(s["s_done"]) == K_SPARTS,
                        "%s overwrote stage %s (tile %s) before S(%s) finished", who, st, j, s["tile"])
             self.check(s["cp_read"], "%s overwrote stage %s (tile %s) before tile %s's chunks 0-3 were copied", who, st, j, s["tile"])
-        self.stage[st] = dict(tile=j, own=False, fwd=False, s_done=set(), cp_read=self.self_recv)
+        self.stage[st] = dict(tile=j, own=False, fwd=False, s_done=set(), cp_read=self.decoupled)
 
     def _delay(self):
         # heavy-tailed: most completions are quick, a few take very long
@@ -219,13 +221,19 @@ class Model:
                 self.check(m["read"], "mask slot %s overwritten before tile %s's softmax", j % 16, m["tile"])
                 self.mask[j % 16] = dict(tile=j, read=False)
             yield ("do", write)
-            # warp 0 arms the value CTA's 16 KB; warps 1-3 arrive
-            yield ("do", lambda st=st, j=j: (self.b(0, "kv_full", st).txop(HALF), self.b(0, "kv_full", st).arrive(tag=j)))
+            # fp8: warp 0 arms the value CTA's 16 KB; the other warps arrive
+            if self.decoupled:
+                yield ("do", lambda st=st, j=j: self.b(0, "kv_full", st).arrive(tag=j))
+            else:
+                yield ("do", lambda st=st, j=j: (self.b(0, "kv_full", st).txop(HALF),
+                                                  self.b(0, "kv_full", st).arrive(tag=j)))
             for _ in range(3):
                 yield ("do", lambda st=st, j=j: self.b(0, "kv_full", st).arrive(tag=j))
 
             def landed(j=j, st=st):
                 self.stage[st]["own"] = True
+                if self.decoupled:      # bf16: the whole tile is this CTA's own load
+                    self.stage[st]["fwd"] = True
                 self.b(0, "kv_loaded", st).arrive(128)
             yield ("do", lambda f=landed: self.later(f))
 
@@ -238,7 +246,7 @@ class Model:
                 o = self.own[os_]
                 self.check(o["fwd_read"] and o["pv_read"],
                            "own slot %s overwritten (tile %s) while tile %s still needed", os_, j, o["tile"])
-                self.own[os_] = dict(tile=j, landed=False, fwd_read=False, pv_read=False, fenced=False)
+                self.own[os_] = dict(tile=j, landed=False, fwd_read=self.decoupled, pv_read=False, fenced=False)
             yield ("do", write)
 
             def landed(j=j, os_=os_):
@@ -267,7 +275,8 @@ class Model:
 
     def score_forwarder(self):
         yield self.W(0, "q_ready", 0, 0)
-        yield ("do", lambda: self.later(lambda: self.b(1, "q_gone", 0).arrive()))
+        if not self.decoupled:
+            yield ("do", lambda: self.later(lambda: self.b(1, "q_gone", 0).arrive()))
         jf = jc = 0
         while jc < self.n:
             moved = False
@@ -279,7 +288,7 @@ class Model:
                     yield ("do", lambda st=st, jf=jf: self.b(0, "kv_full", st).arrive(tag=jf))
                 jf += 1
                 moved = True
-            if self.self_recv:
+            if self.decoupled:
                 jc = jf     # bf16: no copies; the forwarder only fences
             elif jc < jf and self.passed(0, "v_free", jc % K_RECV, jc // K_RECV - 1, "score fwd"):
                 st, rs, j = jc % K_STAGES, jc % K_RECV, jc
@@ -325,7 +334,7 @@ class Model:
     def recv_warp(self):
         for j in range(self.n):
             st, vs, os_ = j % K_STAGES, j % K_RECV, j % K_OWN
-            if not (self.self_recv and self.mut == "recv_skips_v_full"):
+            if not (self.decoupled and self.mut == "recv_skips_v_full"):
                 yield self.W(1, "v_full", vs, j // K_RECV)
 
             def arrivals(st=st, vs=vs, j=j):
@@ -333,7 +342,7 @@ class Model:
                 self.b(1, "v_full", vs).arrive()
                 self.b(1, "s_done", st).arrive(tag=j)
                 self.later(lambda: self.b(0, "s_done", st).arrive(tag=j))
-            if not self.self_recv:
+            if not self.decoupled:
                 yield ("do", arrivals)
             if self.mut != "recv_skips_own_rows":
                 yield self.W(1, "own_loaded", os_, j // K_OWN)
@@ -345,7 +354,7 @@ class Model:
                 if o["tile"] == j and o["landed"]:
                     o["fenced"] = True
                 r = self.recv[vs]
-                if self.self_recv and r["tile"] == j and r["landed"]:
+                if self.decoupled and r["tile"] == j and r["landed"]:
                     r["fenced"] = True
             yield ("do", fence)
             yield ("do", lambda slot=j % K_PSLOTS, j=j: self.b(1, "p_ok", slot).arrive(tag=j))
@@ -511,14 +520,16 @@ class Model:
         return False
 
     def run(self):
-        roles = {"q": self.q_load(), "fwd0": self.score_forwarder(), "fwd1": self.value_forwarder(),
+        roles = {"q": self.q_load(), "fwd0": self.score_forwarder(),
                  "recv": self.recv_warp(), "vmax": self.value_max(), "pv": self.pv_issuer(),
                  "epi": self.epilogue()}
+        if not self.decoupled:
+            roles["fwd1"] = self.value_forwarder()
         for g in (0, 1):
             roles["sp%d" % g] = self.score_producers(g)
             roles["vp%d" % g] = self.value_producers(g)
             roles["sm%d" % g] = self.softmax(g)
-        if self.self_recv:
+        if self.decoupled:
             roles["vp2"] = self.value_recv_producers()
         for b in range(K_SBUF):
             for p in range(K_SPARTS):
@@ -597,5 +608,5 @@ MUTATIONS = {"producers_uncoupled": None, "kv_full_without_fence": None, "produc
              "recv_skips_own_rows": None, "recv_producers_skip_slot_free": True, "recv_skips_v_full": True}
 
 
-def run(ntiles, seed, mutation=None, self_recv=True):
-    Model(ntiles, seed, mutation=mutation, self_recv=self_recv).run()
+def run(ntiles, seed, mutation=None, decoupled=True):
+    Model(ntiles, seed, mutation=mutation, decoupled=decoupled).run()

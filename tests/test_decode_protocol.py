@@ -1,7 +1,8 @@
 """The tensor-core decode's barrier protocol, run under random interleavings
 on the CPU (`tests/decode_protocol_model.py`), in both of its forms (bf16
-cache: the value CTA loads its own chunks 0-3; fp8 cache: the score CTA
-copies them over): every completion order gives no deadlock, no aliased
+cache: each CTA loads what it needs and only P crosses the cluster; fp8
+cache: each CTA forwards the half of the tile its peer lacks): every
+completion order gives no deadlock, no aliased
 parity wait and no buffer overwritten while it is still needed; and each
 planted mistake is caught."""
 import pytest
@@ -12,42 +13,42 @@ TILE_COUNTS = list(range(1, 25)) + [53, 81]
 
 
 FORMS = [True, False]
-FORM_IDS = ["bf16_self_recv", "fp8_copied_recv"]
+FORM_IDS = ["bf16_decoupled", "fp8_copied_recv"]
 
 
-@pytest.mark.parametrize("self_recv", FORMS, ids=FORM_IDS)
+@pytest.mark.parametrize("decoupled", FORMS, ids=FORM_IDS)
 @pytest.mark.parametrize("ntiles", TILE_COUNTS)
-def test_protocol_holds_under_random_completion_order(ntiles, self_recv):
+def test_protocol_holds_under_random_completion_order(ntiles, decoupled):
     for seed in range(25):
-        M.run(ntiles, seed, self_recv=self_recv)
+        M.run(ntiles, seed, decoupled=decoupled)
 
 
-@pytest.mark.parametrize("mutation,self_recv", [(m, f) for m, form in M.MUTATIONS.items() for f in FORMS
+@pytest.mark.parametrize("mutation,decoupled", [(m, f) for m, form in M.MUTATIONS.items() for f in FORMS
                                                 if form is None or form == f])
-def test_planted_protocol_mistake_is_caught(mutation, self_recv):
+def test_planted_protocol_mistake_is_caught(mutation, decoupled):
     for ntiles in (3, 5, 8, 12, 17, 24, 53):
         for seed in range(60):
             try:
-                M.run(ntiles, seed, mutation, self_recv=self_recv)
+                M.run(ntiles, seed, mutation, decoupled=decoupled)
             except M.ProtocolError:
                 return
     pytest.fail("no interleaving exposed the planted mistake %r" % mutation)
 
 
-@pytest.mark.parametrize("self_recv", FORMS, ids=FORM_IDS)
+@pytest.mark.parametrize("decoupled", FORMS, ids=FORM_IDS)
 @pytest.mark.parametrize("own,recv", [(8, 3), (9, 2)])
-def test_other_splits_of_the_value_rings_hold(monkeypatch, own, recv, self_recv):
+def test_other_splits_of_the_value_rings_hold(monkeypatch, own, recv, decoupled):
     # the value CTA's own and receive rings share one region; the kernel's
     # split is 7 + 4, and these fit the same region
     monkeypatch.setattr(M, "K_OWN", own)
     monkeypatch.setattr(M, "K_RECV", recv)
     for ntiles in (1, 2, 5, 9, 16, 23, 54):
         for seed in range(15):
-            M.run(ntiles, seed, self_recv=self_recv)
+            M.run(ntiles, seed, decoupled=decoupled)
 
 
-@pytest.mark.parametrize("self_recv", FORMS, ids=FORM_IDS)
-def test_receive_ring_deeper_than_the_p_slots_is_caught(monkeypatch, self_recv):
+@pytest.mark.parametrize("decoupled", FORMS, ids=FORM_IDS)
+def test_receive_ring_deeper_than_the_p_slots_is_caught(monkeypatch, decoupled):
     # With more receive slots than P slots, the receive warp's p_ok arrival
     # for tile j + 4 can land in tile j's open phase (its receive slot no
     # longer waits for PV(j)), so PV(j) could start before O is rescaled for
@@ -58,7 +59,7 @@ def test_receive_ring_deeper_than_the_p_slots_is_caught(monkeypatch, self_recv):
     for ntiles in (6, 9, 17, 54):
         for seed in range(40):
             try:
-                M.run(ntiles, seed, self_recv=self_recv)
+                M.run(ntiles, seed, decoupled=decoupled)
             except M.ProtocolError as e:
                 assert "mixes arrivals" in str(e)
                 return
